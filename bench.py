@@ -1,0 +1,403 @@
+"""Benchmark of the sparse voxel-grid stencil pipeline on one GB300.
+
+Workload: the sphere shell of radius 185 and thickness 3 (183.5 <= |p| <= 186.5,
+1,290,538 active voxels in 11,255 leaves), fp32 sidecars U[-1,1) with C
+interleaved channels.  One step = the 27-tap box filter (select-based decode +
+cached resolver + streamed gather/accumulate, one fused kernel) over every
+active voxel at C = 1, 3, 8 and 16, BlockWidth 128: four launches.  `value`
+counts each voxel once per channel width: 4 * N voxels per step.
+
+Timing: each launch is bracketed by CUDA events on the launching stream; L2 is
+flushed (a write of twice its size) before every launch, outside the events.
+The step time is the sum of its four launch times.  A JSON line is printed on
+rank 0.  `--impl reference` times the CPU oracle on the host cores instead,
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CS = (1, 3, 8, 16)
+LOG2W = 7
+METRIC = "active voxels/s (27-tap box filter, C=1..16) and achieved HBM GB/s vs GB300 peak"
+WORKLOAD = "S185 sphere shell 183.5<=|p|<=186.5"
+LEAF_META_BYTES = 88  # mask 64 + 9-bit directory 8 + first index 4 + origin 12
+
+
+def algorithmic_bytes(n, n_leaves, n_blocks, W, C):
+    """Unique bytes a launch must move: sidecar rows read, output rows written,
+    leaf metadata and block metadata (tree-node reads excluded)."""
+    return 8 * C * n + 8 * C + LEAF_META_BYTES * n_leaves + (4 + W // 8) * n_blocks
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+
+    import sparse_voxel_grid_gb300 as vbm
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    coords = synth.WORKLOADS["S185"]()
+    g = vbm.vbm_build(coords, LOG2W)
+    info = g.info
+    n, W = info["n_active"], info["block_width"]
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device="cuda")
+
+    sidecars = {C: torch.from_numpy(synth.sidecar_uniform(n, C, seed=0)).cuda() for C in CS}
+    outs = {C: torch.empty_like(sidecars[C]) for C in CS}
+
+    def launch(C, resolver=vbm.RESOLVE_CACHED, output=vbm.OUTPUT_STREAMED, grid=g):
+        vbm.vbm_box_filter(grid, sidecars[C], C, outs[C], resolver, output, stream)
+
+    def timed_launch(fn):
+        flush_buf.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        return e0, e1
+
+    # warm-up
+    for _ in range(args.warmup):
+        for C in CS:
+            timed_launch(lambda C=C: launch(C))
+    torch.cuda.synchronize()
+
+    # timed region
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        evs = {C: [] for C in CS}
+        for _ in range(args.steps):
+            for C in CS:
+                evs[C].append(timed_launch(lambda C=C: launch(C)))
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+    per_c_ms = {C: [a.elapsed_time(b) for a, b in evs[C]] for C in CS}
+    step_ms = [sum(per_c_ms[C][k] for C in CS) for k in range(args.steps)]
+    ms_per_step = statistics.mean(step_ms)
+    if dist:
+        t = torch.tensor([ms_per_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * len(CS) * n / (ms_per_step * 1e-3)
+
+    peak_gbs, peak_kind = peaks()
+    detail = {}
+    for C in CS:
+        ms = statistics.mean(per_c_ms[C])
+        b = algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, C)
+        detail[f"C{C}"] = {"ms_mean": round(ms, 5), "ms_median": round(statistics.median(per_c_ms[C]), 5),
+                           "ms_min": round(min(per_c_ms[C]), 5), "voxels_per_s": n / (ms * 1e-3),
+                           "alg_bytes": b, "gbs": b / (ms * 1e-3) / 1e9,
+                           "frac_of_hbm": b / (ms * 1e-3) / 1e9 / peak_gbs}
+    dom = max(CS, key=lambda C: statistics.mean(per_c_ms[C]))
+    dom_ms = statistics.mean(per_c_ms[dom])
+    dom_bytes = algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, dom)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = load_traffic(f"box_cached_streamed_C{dom}")
+
+    # end to end through the public API: pinned host sidecar -> device -> filter -> host
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, vbm, g, n, sidecars, outs, args, stream)
+
+    variants = run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args) if not args.no_variants else None
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(coords, sample=args.cpu_sample)
+
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": f"{WORKLOAD}, N={n}, leaves={info['n_leaves']}, fused decode + cached resolver + "
+                               f"streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
+                   "n_active": n, "n_leaves": info["n_leaves"], "block_width": W, "channels": list(CS),
+                   "resolver": "cached", "output": "streamed", "l2": "flushed before every launch",
+                   "value_counts": "4*N voxels per step (one per channel width)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
+        "roofline": {"bound": "hbm", "kernel": f"box_filter cached streamed C={dom}", "achieved": achieved,
+                     "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes},
+        "detail": detail,
+        "e2e": e2e,
+        "gpu_launches": len(CS) * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "variants": variants,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def load_traffic(key):
+    """DRAM bytes per launch from a committed ncu summary, if it covers `key`
+    for the current kernel version."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    return d.get(key)
+
+
+def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream):
+    host_in = {C: sidecars[C].cpu().pin_memory() for C in CS}
+    host_out = {C: torch.empty_like(host_in[C]).pin_memory() for C in CS}
+    dev_in = {C: torch.empty_like(sidecars[C]) for C in CS}
+
+    def step():
+        for C in CS:
+            dev_in[C].copy_(host_in[C], non_blocking=True)
+            vbm.vbm_box_filter(g, dev_in[C], C, outs[C], vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED, stream)
+            host_out[C].copy_(outs[C], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    bi = sum(host_in[C].numel() * 4 for C in CS)
+    bo = sum(host_out[C].numel() * 4 for C in CS)
+    return {"value": len(CS) * n / (ms * 1e-3), "unit": "voxels/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
+    """Every box variant (resolver x output x W x C), the cross Laplacian and
+    the decode on the shell, each timed cold-cache (mean of a few launches)."""
+    reps = args.variant_reps
+    res = []
+
+    def tmean(fn):
+        for _ in range(2):
+            timed_launch(fn)
+        evs = [timed_launch(fn) for _ in range(reps)]
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    for log2w in (7, 9):
+        g = vbm.vbm_build(coords, log2w)
+        for C in CS:
+            for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED)):
+                for oname, o in (("streamed", vbm.OUTPUT_STREAMED), ("materialised", vbm.OUTPUT_MATERIALISED)):
+                    ms = tmean(lambda: vbm.vbm_box_filter(g, sidecars[C], C, outs[C], r, o))
+                    res.append({"kernel": "box", "W": 1 << log2w, "C": C, "resolver": rname, "output": oname,
+                                "ms": round(ms, 5)})
+        g.close()
+    for log2w in (6, 7, 8, 9):
+        g = vbm.vbm_build(coords, log2w)
+        for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED)):
+            ms = tmean(lambda: vbm.vbm_cross_filter(g, sidecars[1], 1, outs[1], r, vbm.CROSS_LAPLACIAN))
+            res.append({"kernel": "laplacian", "W": 1 << log2w, "C": 1, "resolver": rname, "ms": round(ms, 5)})
+        li = torch.empty(g.n_slots, dtype=torch.int32, device="cuda")
+        vo = torch.empty(g.n_slots, dtype=torch.int16, device="cuda")
+        ms = tmean(lambda: vbm.vbm_decode(g, li, vo))
+        res.append({"kernel": "decode", "W": 1 << log2w, "ms": round(ms, 5)})
+        g.close()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(coords, sample):
+    import oracle
+    import synth
+
+    t0 = time.perf_counter()
+    o = oracle.OracleGrid(coords)
+    t_build = time.perf_counter() - t0
+    which = np.arange(1, min(sample, o.n) + 1, dtype=np.int64)
+    t = 0.0
+    for C in CS:
+        s = synth.sidecar_uniform(o.n, C, seed=0)
+        t0 = time.perf_counter()
+        o.box_filter(s, C, which=which)
+        t += time.perf_counter() - t0
+    return {"value": len(CS) * len(which) / t, "unit": "voxels/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {len(which)} of {o.n} voxels of the shell at C=1,3,8,16 "
+                      f"(single-threaded C++ oracle; index build {t_build:.2f} s not counted)",
+            "seconds": t}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    coords = synth.WORKLOADS["S185"]()
+    o = oracle.OracleGrid(coords)
+    sides = {C: synth.sidecar_uniform(o.n, C, seed=0) for C in CS}
+    # Size the per-step sample so that warm-up + timed steps take about
+    # --reference-seconds in total (calibrated on 2000 voxels).
+    probe = np.arange(1, min(2000, o.n) + 1, dtype=np.int64)
+    t0 = time.perf_counter()
+    for C in CS:
+        o.box_filter(sides[C], C, which=probe)
+    per_voxel = (time.perf_counter() - t0) / len(probe)
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    m = int(min(args.cpu_sample, o.n, max(2000, budget / per_voxel)))
+    which = np.arange(1, m + 1, dtype=np.int64)
+
+    def step():
+        for C in CS:
+            o.box_filter(sides[C], C, which=which)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = len(CS) * len(which) / dt
+    sample = f"first {len(which)} of {o.n} voxels of the shell per step, C=1,3,8,16 (single-threaded C++ oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": f"{WORKLOAD}, N={o.n}, 27-tap box filter at C=1,3,8,16", "n_active": o.n,
+                   "channels": list(CS), "sample_voxels": len(which)},
+        "cpu_baseline": {"value": value, "unit": "voxels/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-sample", type=int, default=150000)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--variant-reps", type=int, default=5)
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

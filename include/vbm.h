@@ -1,0 +1,179 @@
+/*
+ * vbm.h -- C ABI of libvbm.so, a GB300 (sm_103a) sparse voxel-grid stencil
+ * library in the style of NanoVDB's VoxelBlockManager (VBM).
+ *
+ * Sources (web pages; cited by title and section):
+ *   [2263] OpenVDB PR #2263 "Alternative stencil resolvers for VoxelBlockManager"
+ *   [2262] OpenVDB PR #2262 "NanoVDB VBM: Streaming box-stencil"
+ *   [2258] OpenVDB PR #2258 "VBM select-based inverse-map decode"
+ *
+ * Model.  An index grid ([2262] "What changed") maps each of N active voxels
+ * to an index 1..N into a caller-owned sidecar; index 0 means background.  The
+ * grid is a sparse tree of 8^3 leaves (512-bit value masks with a 9-bit
+ * per-word prefix-sum directory, [2258] "Summary") under 16^3 lower and 32^3
+ * upper nodes and a root table.  Indices are assigned in depth-first tree order:
+ * upper nodes by signed (x>>12, y>>12, z>>12) lexicographically, then lower-node
+ * slot, leaf slot and in-leaf offset off = (x&7)*64 + (y&7)*8 + (z&7), each slot
+ * x-major.  The VBM cuts the index range into blocks of W = 2^log2 consecutive
+ * indices (block b holds 1+b*W .. (b+1)*W); per block it stores firstLeafID
+ * (leaf of the block's first index) and jumpMap (bit s, 1 <= s < W, set iff
+ * index 1+b*W+s starts a leaf) ([2263] "Built on the register-decode API").
+ *
+ * Conventions for every call.
+ *   - Return value: VBM_OK (0) or a negative VBM_ERR_* code; vbm_last_error()
+ *     returns a text for the calling thread's last failure.  No call throws,
+ *     traps or aborts.
+ *   - Device pointers are caller-owned (e.g. torch allocations) and must point
+ *     to memory on the device that was current when the grid was built; they
+ *     must be 16-byte aligned.  A grid handle owns only its own arrays.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute
+ *     calls only enqueue work: they return after launching, and launch errors
+ *     are reported as VBM_ERR_CUDA.  Results are ready when the stream is.
+ *   - Sidecars and filter outputs hold (N+1) rows of C interleaved fp32
+ *     channels: row r at [r*C, r*C+C).  Row 0 (background) is never read as a
+ *     tap; filters write it as +0.0 so an output can serve as the next sidecar.
+ *     Rows of a filter output are written only by that call: out must not
+ *     alias the sidecar.
+ *   - Limits: N < 2^31 (indices are 32-bit), |x|,|y|,|z| <= 2^30, C in 1..64,
+ *     log2 block width in 6..9 (W = 64..512).
+ */
+#ifndef VBM_H
+#define VBM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define VBM_OK 0
+#define VBM_ERR_INVALID (-1)   /* NULL pointer, unknown enum, C or log2 width out of range */
+#define VBM_ERR_DUPLICATE (-2) /* a coordinate appears twice and VBM_BUILD_DEDUP was not given */
+#define VBM_ERR_RANGE (-3)     /* N or a coordinate beyond the limits above */
+#define VBM_ERR_NOMEM (-4)     /* host or device allocation failed */
+#define VBM_ERR_CUDA (-5)      /* a CUDA runtime call or kernel launch failed */
+#define VBM_ERR_ALIGN (-6)     /* a device pointer is not 16-byte aligned */
+#define VBM_ERR_STATE (-7)     /* grid was built with VBM_BUILD_HOST_ONLY (no device arrays) */
+
+/* MaxCachedLeaves: a block whose indices span more leaves than this resolves
+ * its taps by tree walk instead of the cached table ([2263] "Notes":
+ * MaxCachedLeaves is 16; "Summary": blocks spanning more fall back to per-tap
+ * traversal). */
+#define VBM_MAX_CACHED_LEAVES 16
+
+/* vbm_build flags */
+#define VBM_BUILD_DEDUP 1u     /* drop repeated coordinates instead of failing */
+#define VBM_BUILD_HOST_ONLY 2u /* build the host arrays only (no CUDA calls); for inspection */
+
+/* resolver: how a tap's index is found ([2263] "Summary" table) */
+#define VBM_RESOLVE_TREEWALK 0 /* root-down tree traversal per tap; no shared memory */
+#define VBM_RESOLVE_CACHED 1   /* per-block neighbour-leaf table staged in shared memory */
+
+/* output: how taps reach the consumer ([2262] "Summary", [2263] "Summary") */
+#define VBM_OUTPUT_STREAMED 0     /* each (tap, index) consumed as it is resolved (forEach*) */
+#define VBM_OUTPUT_MATERIALISED 1 /* all taps resolved into a per-thread array first (compute*) */
+
+/* cross-stencil consumer */
+#define VBM_CROSS_LAPLACIAN 0 /* sum of the active face values (increasing tap order) - 6*centre */
+#define VBM_CROSS_SUM 1       /* sum of the 7 taps' values in tap order */
+
+/* vbm_leaf_export: which host array */
+#define VBM_EXPORT_LEAF_MASK 0    /* n_leaves x 8 uint64: value masks, bit off%64 of word off/64 */
+#define VBM_EXPORT_LEAF_PREFIX 1  /* n_leaves uint64: 9-bit field w-1 (w=1..7) = set bits in words 0..w-1 */
+#define VBM_EXPORT_LEAF_FIRST 2   /* n_leaves uint32: index of the leaf's first active voxel */
+#define VBM_EXPORT_LEAF_ORIGIN 3  /* n_leaves x 3 int32: leaf origin (multiple of 8) */
+#define VBM_EXPORT_BLOCK_FIRST_LEAF 4 /* n_blocks uint32: firstLeafID */
+#define VBM_EXPORT_BLOCK_JUMP 5   /* n_blocks x (W/64) uint64: jumpMap, bit s in word s/64 */
+
+typedef struct vbm_grid vbm_grid;
+
+typedef struct vbm_info_t {
+    uint64_t n_active;            /* N */
+    uint64_t n_leaves;
+    uint64_t n_blocks;            /* ceil(N / W) */
+    uint32_t block_width;         /* W */
+    uint32_t log2_block_width;
+    uint32_t n_upper;             /* 32^3 upper nodes */
+    uint32_t n_lower;             /* 16^3 lower nodes */
+    uint64_t n_blocks_over_cache; /* blocks spanning > VBM_MAX_CACHED_LEAVES leaves (tree-walk fallback) */
+    uint32_t max_span;            /* most leaves any block spans (1 + popcount(jumpMap)) */
+    uint32_t on_device;           /* 1 if device arrays exist */
+    uint64_t device_bytes;        /* bytes of device memory the grid owns */
+} vbm_info_t;
+
+/* Text of the calling thread's last error ("" if none).  Valid until the
+ * thread's next vbm_* call. */
+const char* vbm_last_error(void);
+
+/* Build the index grid and VBM block metadata from N active coordinates
+ * (host array, coords[3*i .. 3*i+2] = x,y,z of voxel i, any order).  Uploads
+ * the grid to the current device with copies on `stream` and synchronises the
+ * stream before returning, so `coords` may be freed afterwards.  *out receives
+ * a new handle (release with vbm_destroy).  N = 0 gives an empty grid.
+ * Errors: INVALID (out NULL, coords NULL with n > 0, bad log2 width or flags),
+ * RANGE, DUPLICATE, NOMEM, CUDA.  The index assignment and metadata follow
+ * the model above ([2258] "Summary": the leaf mask, its 9-bit directory and
+ * the block's jumpMap are what the decode reads). */
+int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
+              vbm_grid** out);
+
+/* Free a grid and its device arrays.  NULL is accepted.  The caller must make
+ * sure no launched work still uses the grid (synchronise its streams first). */
+int vbm_destroy(vbm_grid* grid);
+
+/* Sizes and statistics of a grid.  Errors: INVALID. */
+int vbm_info(const vbm_grid* grid, vbm_info_t* info);
+
+/* Copy one of the grid's host-side arrays (see VBM_EXPORT_*) into dst, which
+ * holds `bytes` bytes; the exact size is required.  Errors: INVALID, RANGE
+ * (bytes differs from the array's size). */
+int vbm_leaf_export(const vbm_grid* grid, int what, void* dst, uint64_t bytes);
+
+/* Select-based inverse-map decode ([2258] "What changed"): for every slot of
+ * every block, leaf_index[b*W+s] = firstLeafID[b] + popcount(jumpMap[b] bits
+ * 0..s) and voxel_offset[b*W+s] = position of the r-th set bit of that leaf's
+ * mask (r = index - the leaf's first index), found through the 9-bit prefix
+ * directory and an in-word select.  Slots whose index 1+b*W+s exceeds N get
+ * the sentinels leaf_index = 0xFFFFFFFF, voxel_offset = 0xFFFF ([2258]
+ * "Validation").  Both outputs are device arrays of n_blocks*W entries.
+ * Errors: INVALID, STATE, ALIGN, CUDA. */
+int vbm_decode(const vbm_grid* grid, uint32_t* leaf_index, uint16_t* voxel_offset, void* stream);
+
+/* 27-tap box filter ([2262] "What changed", "A/B"; [2263] "Measurements"): for
+ * every active voxel v and channel ch,
+ *     out[v*C+ch] = sum over taps t = (di+1)*9+(dj+1)*3+(dk+1), t = 0..26, of
+ *                   sidecar[idx_t*C+ch] for each tap whose index idx_t != 0,
+ * accumulated in fp32 from +0.0 in increasing t with round-to-nearest adds (no
+ * reassociation), so every resolver/output combination gives the same bits.
+ * Each slot is decoded in registers, its taps resolved by `resolver`
+ * (VBM_RESOLVE_*) and consumed per `output` (VBM_OUTPUT_*); blocks spanning more
+ * than VBM_MAX_CACHED_LEAVES leaves use the tree walk.  sidecar and out are
+ * device arrays of (N+1)*C floats.  Errors: INVALID, STATE, ALIGN, CUDA. */
+int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out, int resolver, int output,
+                   void* stream);
+
+/* 7-tap cross stencil (centre and the six face neighbours, taps t in
+ * {4,10,12,13,14,16,22} of the box numbering) consumed as `op`:
+ * VBM_CROSS_LAPLACIAN: out = s - 6*centre, s = +0.0 plus each active face
+ * value in increasing t, the product and the difference rounded separately;
+ * VBM_CROSS_SUM: the plain fp32 sum of the active taps' values in tap order.
+ * Taps are materialised per thread, as in the pages' compute*CrossStencil*
+ * ([2263] "Notes": there is no streaming cross resolver).  Errors as for
+ * vbm_box_filter. */
+int vbm_cross_filter(const vbm_grid* grid, const float* sidecar, int C, float* out, int resolver, int op,
+                     void* stream);
+
+/* Raw taps for byte-exact validation ([2263] "Validation": all taps of every
+ * thread materialised to global memory): taps[v*27 + t] (box) or taps[v*7 + j]
+ * (cross) is the index of that neighbour of voxel v, 0 if inactive; row 0 is
+ * all zeros.  taps is a device array of (N+1)*27 or (N+1)*7 uint32.
+ * Errors: INVALID, STATE, ALIGN, CUDA. */
+int vbm_box_taps(const vbm_grid* grid, uint32_t* taps, int resolver, void* stream);
+int vbm_cross_taps(const vbm_grid* grid, uint32_t* taps, int resolver, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VBM_H */

@@ -1,0 +1,295 @@
+// C ABI of libvbm.so (declared in include/vbm.h): argument checks, the grid's
+// device arena, and dispatch to the kernel launchers.  Every entry point
+// returns a status code; nothing throws across the boundary.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "vbm_internal.h"
+#include "vbm_launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int fail_cuda(const char* what, cudaError_t e) {
+    return fail(VBM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Switches to the grid's device for the duration of a call.
+class DeviceGuard {
+   public:
+    explicit DeviceGuard(int device) {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        if (prev_ != device) ok_ = cudaSetDevice(device) == cudaSuccess; else prev_ = -1;
+    }
+    ~DeviceGuard() {
+        if (prev_ >= 0) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+   private:
+    int prev_ = -1;
+    bool ok_ = true;
+};
+
+// Copies the host arrays into one device allocation and fills g->dev.
+int upload(vbm_grid* g, cudaStream_t stream) {
+    struct Part {
+        const void* src;
+        size_t bytes;
+        size_t off;
+    };
+    Part parts[6] = {
+        {g->leaves.data(), g->leaves.size() * sizeof(vbm::LeafRec), 0},
+        {g->root_keys.data(), g->root_keys.size() * sizeof(uint64_t), 0},
+        {g->upper.data(), g->upper.size() * sizeof(uint32_t), 0},
+        {g->lower.data(), g->lower.size() * sizeof(uint32_t), 0},
+        {g->first_leaf.data(), g->first_leaf.size() * sizeof(uint32_t), 0},
+        {g->jump.data(), g->jump.size() * sizeof(uint64_t), 0},
+    };
+    size_t total = 0;
+    for (Part& p : parts) {
+        p.off = total;
+        total = round_up(total + p.bytes, 256);
+    }
+    total = total ? total : 256;
+    cudaError_t e = cudaGetDevice(&g->device);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: cudaGetDevice", e);
+    e = cudaMalloc(&g->arena, total);
+    if (e != cudaSuccess) {
+        g->arena = nullptr;
+        cudaGetLastError();
+        return fail(VBM_ERR_NOMEM, std::string("vbm_build: cudaMalloc of ") + std::to_string(total) +
+                                       " bytes failed: " + cudaGetErrorString(e));
+    }
+    g->arena_bytes = total;
+    char* base = static_cast<char*>(g->arena);
+    for (const Part& p : parts) {
+        if (!p.bytes) continue;
+        e = cudaMemcpyAsync(base + p.off, p.src, p.bytes, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return fail_cuda("vbm_build: cudaMemcpyAsync", e);
+    }
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);
+    vbm::DevGrid& d = g->dev;
+    d.leaves = reinterpret_cast<const vbm::LeafRec*>(base + parts[0].off);
+    d.root_keys = reinterpret_cast<const uint64_t*>(base + parts[1].off);
+    d.upper = reinterpret_cast<const uint32_t*>(base + parts[2].off);
+    d.lower = reinterpret_cast<const uint32_t*>(base + parts[3].off);
+    d.first_leaf = reinterpret_cast<const uint32_t*>(base + parts[4].off);
+    d.jump = reinterpret_cast<const uint64_t*>(base + parts[5].off);
+    d.n = (uint32_t)g->n;
+    d.n_leaves = (uint32_t)g->n_leaves;
+    d.n_blocks = (uint32_t)g->n_blocks;
+    d.n_upper = g->n_upper;
+    d.log2w = g->log2w;
+    return VBM_OK;
+}
+
+// Common checks for the compute calls.
+int check_grid(const vbm_grid* g, const char* fn) {
+    if (!g) return fail(VBM_ERR_INVALID, std::string(fn) + ": grid is NULL");
+    if (!g->arena) return fail(VBM_ERR_STATE, std::string(fn) + ": grid was built host-only (no device arrays)");
+    return VBM_OK;
+}
+
+int check_ptr(const void* p, const char* fn, const char* name) {
+    if (!p) return fail(VBM_ERR_INVALID, std::string(fn) + ": " + name + " is NULL");
+    if (!aligned16(p)) return fail(VBM_ERR_ALIGN, std::string(fn) + ": " + name + " is not 16-byte aligned");
+    return VBM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vbm_last_error(void) { return g_last_error.c_str(); }
+
+int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
+              vbm_grid** out) {
+    g_last_error.clear();
+    if (!out) return fail(VBM_ERR_INVALID, "vbm_build: out is NULL");
+    *out = nullptr;
+    if (!coords && n) return fail(VBM_ERR_INVALID, "vbm_build: coords is NULL");
+    if (log2_block_width < 6 || log2_block_width > 9)
+        return fail(VBM_ERR_INVALID, "vbm_build: log2_block_width must be in 6..9");
+    if (flags & ~(VBM_BUILD_DEDUP | VBM_BUILD_HOST_ONLY)) return fail(VBM_ERR_INVALID, "vbm_build: unknown flags");
+    vbm_grid* g = new (std::nothrow) vbm_grid;
+    if (!g) return fail(VBM_ERR_NOMEM, "vbm_build: out of host memory");
+    int rc;
+    try {
+        std::string err;
+        rc = vbm::build_host(coords, n, log2_block_width, flags, g, err);
+        if (rc != VBM_OK) {
+            delete g;
+            return fail(rc, err);
+        }
+    } catch (const std::bad_alloc&) {
+        delete g;
+        return fail(VBM_ERR_NOMEM, "vbm_build: out of host memory");
+    }
+    if (!(flags & VBM_BUILD_HOST_ONLY)) {
+        rc = upload(g, static_cast<cudaStream_t>(stream));
+        if (rc != VBM_OK) {
+            std::string msg = g_last_error;
+            vbm_destroy(g);
+            return fail(rc, msg);
+        }
+    }
+    *out = g;
+    return VBM_OK;
+}
+
+int vbm_destroy(vbm_grid* g) {
+    g_last_error.clear();
+    if (!g) return VBM_OK;
+    int rc = VBM_OK;
+    if (g->arena) {
+        DeviceGuard guard(g->device);
+        cudaError_t e = cudaFree(g->arena);
+        if (e != cudaSuccess) rc = fail_cuda("vbm_destroy: cudaFree", e);
+    }
+    delete g;
+    return rc;
+}
+
+int vbm_info(const vbm_grid* g, vbm_info_t* info) {
+    g_last_error.clear();
+    if (!g || !info) return fail(VBM_ERR_INVALID, "vbm_info: NULL argument");
+    std::memset(info, 0, sizeof(*info));
+    info->n_active = g->n;
+    info->n_leaves = g->n_leaves;
+    info->n_blocks = g->n_blocks;
+    info->block_width = 1u << g->log2w;
+    info->log2_block_width = (uint32_t)g->log2w;
+    info->n_upper = g->n_upper;
+    info->n_lower = g->n_lower;
+    info->n_blocks_over_cache = g->n_over_cache;
+    info->max_span = g->max_span;
+    info->on_device = g->arena ? 1u : 0u;
+    info->device_bytes = g->arena_bytes;
+    return VBM_OK;
+}
+
+int vbm_leaf_export(const vbm_grid* g, int what, void* dst, uint64_t bytes) {
+    g_last_error.clear();
+    if (!g || (!dst && bytes)) return fail(VBM_ERR_INVALID, "vbm_leaf_export: NULL argument");
+    const size_t nl = g->leaves.size();
+    size_t need = 0;
+    switch (what) {
+        case VBM_EXPORT_LEAF_MASK: need = nl * 8 * sizeof(uint64_t); break;
+        case VBM_EXPORT_LEAF_PREFIX: need = nl * sizeof(uint64_t); break;
+        case VBM_EXPORT_LEAF_FIRST: need = nl * sizeof(uint32_t); break;
+        case VBM_EXPORT_LEAF_ORIGIN: need = nl * 3 * sizeof(int32_t); break;
+        case VBM_EXPORT_BLOCK_FIRST_LEAF: need = g->first_leaf.size() * sizeof(uint32_t); break;
+        case VBM_EXPORT_BLOCK_JUMP: need = g->jump.size() * sizeof(uint64_t); break;
+        default: return fail(VBM_ERR_INVALID, "vbm_leaf_export: unknown array");
+    }
+    if (bytes != need)
+        return fail(VBM_ERR_RANGE, "vbm_leaf_export: expected " + std::to_string(need) + " bytes, got " +
+                                       std::to_string(bytes));
+    char* out = static_cast<char*>(dst);
+    for (size_t l = 0; l < nl; ++l) {
+        const vbm::LeafRec& r = g->leaves[l];
+        switch (what) {
+            case VBM_EXPORT_LEAF_MASK: std::memcpy(out + l * 64, r.mask, 64); break;
+            case VBM_EXPORT_LEAF_PREFIX: std::memcpy(out + l * 8, &r.prefix, 8); break;
+            case VBM_EXPORT_LEAF_FIRST: std::memcpy(out + l * 4, &r.first, 4); break;
+            case VBM_EXPORT_LEAF_ORIGIN: std::memcpy(out + l * 12, r.origin, 12); break;
+            default: break;
+        }
+    }
+    if (what == VBM_EXPORT_BLOCK_FIRST_LEAF && need) std::memcpy(out, g->first_leaf.data(), need);
+    if (what == VBM_EXPORT_BLOCK_JUMP && need) std::memcpy(out, g->jump.data(), need);
+    return VBM_OK;
+}
+
+int vbm_decode(const vbm_grid* g, uint32_t* leaf_index, uint16_t* voxel_offset, void* stream) {
+    g_last_error.clear();
+    int rc = check_grid(g, "vbm_decode");
+    if (rc) return rc;
+    if (g->n_blocks == 0) return VBM_OK;
+    if ((rc = check_ptr(leaf_index, "vbm_decode", "leaf_index"))) return rc;
+    if ((rc = check_ptr(voxel_offset, "vbm_decode", "voxel_offset"))) return rc;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_decode: cannot select the grid's device");
+    cudaError_t e = vbm::launch_decode(g->dev, leaf_index, voxel_offset, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_decode: launch", e);
+}
+
+static int check_filter(const vbm_grid* g, const float* sidecar, int C, const float* out, int resolver,
+                        const char* fn) {
+    int rc = check_grid(g, fn);
+    if (rc) return rc;
+    if (C < 1 || C > vbm::kMaxC) return fail(VBM_ERR_INVALID, std::string(fn) + ": C must be in 1..64");
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED)
+        return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
+    if ((rc = check_ptr(sidecar, fn, "sidecar"))) return rc;
+    if ((rc = check_ptr(out, fn, "out"))) return rc;
+    if ((const void*)sidecar == (const void*)out) return fail(VBM_ERR_INVALID, std::string(fn) + ": out aliases sidecar");
+    return VBM_OK;
+}
+
+int vbm_box_filter(const vbm_grid* g, const float* sidecar, int C, float* out, int resolver, int output,
+                   void* stream) {
+    g_last_error.clear();
+    int rc = check_filter(g, sidecar, C, out, resolver, "vbm_box_filter");
+    if (rc) return rc;
+    if (output != VBM_OUTPUT_STREAMED && output != VBM_OUTPUT_MATERIALISED)
+        return fail(VBM_ERR_INVALID, "vbm_box_filter: unknown output mode");
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_box_filter: cannot select the grid's device");
+    cudaError_t e = vbm::launch_box_filter(g->dev, sidecar, C, out, resolver, output, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter: launch", e);
+}
+
+int vbm_cross_filter(const vbm_grid* g, const float* sidecar, int C, float* out, int resolver, int op,
+                     void* stream) {
+    g_last_error.clear();
+    int rc = check_filter(g, sidecar, C, out, resolver, "vbm_cross_filter");
+    if (rc) return rc;
+    if (op != VBM_CROSS_LAPLACIAN && op != VBM_CROSS_SUM)
+        return fail(VBM_ERR_INVALID, "vbm_cross_filter: unknown op");
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_cross_filter: cannot select the grid's device");
+    cudaError_t e = vbm::launch_cross_filter(g->dev, sidecar, C, out, resolver, op, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_cross_filter: launch", e);
+}
+
+static int taps_common(const vbm_grid* g, uint32_t* taps, int resolver, void* stream, bool box) {
+    const char* fn = box ? "vbm_box_taps" : "vbm_cross_taps";
+    int rc = check_grid(g, fn);
+    if (rc) return rc;
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED)
+        return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
+    if ((rc = check_ptr(taps, fn, "taps"))) return rc;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = box ? vbm::launch_box_taps(g->dev, taps, resolver, s) : vbm::launch_cross_taps(g->dev, taps, resolver, s);
+    return e == cudaSuccess ? VBM_OK : fail_cuda((std::string(fn) + ": launch").c_str(), e);
+}
+
+int vbm_box_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) {
+    g_last_error.clear();
+    return taps_common(g, taps, resolver, stream, true);
+}
+
+int vbm_cross_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) {
+    g_last_error.clear();
+    return taps_common(g, taps, resolver, stream, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,221 @@
+// 27-tap box stencil: fused decode + resolve + gather/accumulate filter, and
+// the raw-tap export used for byte-exact validation.
+//
+// Sources (web pages; cited by title and section):
+//   [2263] OpenVDB PR #2263 "Alternative stencil resolvers for VoxelBlockManager"
+//   [2262] OpenVDB PR #2262 "NanoVDB VBM: Streaming box-stencil"
+//
+// One CTA per VBM block, one thread per slot.  Each thread decodes its slot in
+// registers, resolves the 27 taps in order t = (di+1)*9 + (dj+1)*3 + (dk+1)
+// ([2262] "What changed") either by tree walk or through the block's cached
+// neighbour-leaf table ([2263] "Summary"), and for each non-zero tap adds
+// sidecar[idx*C + ch] to a per-channel fp32 accumulator that starts at +0.0.
+// Streamed: each tap is consumed as soon as it is resolved (forEachBoxStencil);
+// materialised: all 27 indices are resolved into a per-thread array first
+// (computeBoxStencil).  Both add the same values in the same order, so the
+// results are identical bit for bit ([2262] "Validation").
+#include "vbm_device.cuh"
+#include "vbm_launch.h"
+
+namespace vbm {
+namespace {
+
+// acc[ch] += sidecar[idx*C + ch0 + ch] for ch < CC; VEC: the row is read as
+// float4s (CC % 4 == 0 and rows 16-byte aligned).
+template <int CC, bool VEC>
+__device__ __forceinline__ void gather_add(float (&acc)[CC], const float* __restrict__ sc, uint32_t idx, int C,
+                                           int ch0) {
+    const float* row = sc + (size_t)idx * (size_t)C + ch0;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int q = 0; q < CC / 4; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
+            acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], v.x);
+            acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], v.y);
+            acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
+            acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], v.w);
+        }
+    } else {
+#pragma unroll
+        for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], __ldg(row + ch));
+    }
+}
+
+template <int CC, bool VEC>
+__device__ __forceinline__ void store_row(float* __restrict__ out, uint32_t index, int C, int ch0,
+                                          const float (&acc)[CC]) {
+    float* row = out + (size_t)index * (size_t)C + ch0;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int q = 0; q < CC / 4; ++q)
+            reinterpret_cast<float4*>(row)[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int ch = 0; ch < CC; ++ch) row[ch] = acc[ch];
+    }
+}
+
+// Resolves tap (di,dj,dk) of one decoded voxel.  TABLE: through the block's
+// staged neighbour-leaf table row of the voxel's leaf; otherwise by tree walk.
+template <bool TABLE>
+struct TapResolver {
+    const DevGrid* g;
+    const uint32_t* row;     // TABLE: 27 neighbour-leaf ids of the voxel's leaf
+    int32_t x, y, z;         // TABLE: in-leaf position (0..7); walk: absolute coordinate
+
+    __device__ __forceinline__ TapResolver(const DevGrid& grid, const uint32_t* table_row, const Slot& d) : g(&grid) {
+        const int32_t lx = (int32_t)(d.off >> 6), ly = (int32_t)((d.off >> 3) & 7u), lz = (int32_t)(d.off & 7u);
+        if constexpr (TABLE) {
+            row = table_row;
+            x = lx; y = ly; z = lz;
+        } else {
+            row = nullptr;
+            const LeafRec* r = grid.leaves + d.leaf;
+            x = __ldg(&r->origin[0]) + lx;
+            y = __ldg(&r->origin[1]) + ly;
+            z = __ldg(&r->origin[2]) + lz;
+        }
+    }
+    __device__ __forceinline__ uint32_t operator()(int di, int dj, int dk) const {
+        if constexpr (TABLE) return cached_index(g->leaves, row, x + di, y + dj, z + dk);
+        else return walk_index(*g, x + di, y + dj, z + dk);
+    }
+};
+
+template <int CC, bool VEC, bool TABLE, bool MAT>
+__device__ __forceinline__ void box_slot(const DevGrid& g, const uint32_t* table_row, const Slot& d, uint32_t index,
+                                         const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
+    const TapResolver<TABLE> resolve(g, table_row, d);
+    float acc[CC];
+#pragma unroll
+    for (int ch = 0; ch < CC; ++ch) acc[ch] = 0.0f;
+    if constexpr (MAT) {
+        uint32_t st[kBoxTaps];
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t) st[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t)
+            if (st[t]) gather_add<CC, VEC>(acc, sc, st[t], C, ch0);
+    } else {
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t) {
+            const uint32_t idx = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
+            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
+        }
+    }
+    store_row<CC, VEC>(out, index, C, ch0, acc);
+}
+
+template <int CC, bool VEC, bool CACHED, bool MAT>
+__global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float* __restrict__ sc,
+                                                         float* __restrict__ out, int C, int ch0) {
+    __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kBoxTaps : 1];
+    const uint32_t W = 1u << g.log2w, words = W >> 6;
+    const uint32_t b = blockIdx.x;
+    const uint64_t* jb = g.jump + (size_t)b * words;
+    const uint32_t fl = __ldg(&g.first_leaf[b]);
+    bool use_table = false;
+    if constexpr (CACHED) {
+        const uint32_t span = block_span(jb, words);
+        use_table = span <= VBM_MAX_CACHED_LEAVES;  // block-uniform: the barrier inside is safe
+        if (use_table) stage_leaf_table(g, fl, span, table);
+    }
+    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
+        const uint32_t index = 1u + b * W + s;
+        if (index > g.n) break;
+        const Slot d = decode_slot(g, fl, jb, s, index);
+        if constexpr (CACHED) {
+            if (use_table) {
+                box_slot<CC, VEC, true, MAT>(g, table + (d.leaf - fl) * kBoxTaps, d, index, sc, out, C, ch0);
+                continue;
+            }
+        }
+        box_slot<CC, VEC, false, MAT>(g, nullptr, d, index, sc, out, C, ch0);
+    }
+    if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
+}
+
+// Raw taps: taps[index*27 + t].  Row 0 is zero.
+template <bool CACHED>
+__global__ void __launch_bounds__(512) box_taps_kernel(DevGrid g, uint32_t* __restrict__ taps) {
+    __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kBoxTaps : 1];
+    const uint32_t W = 1u << g.log2w, words = W >> 6;
+    const uint32_t b = blockIdx.x;
+    const uint64_t* jb = g.jump + (size_t)b * words;
+    const uint32_t fl = __ldg(&g.first_leaf[b]);
+    bool use_table = false;
+    if constexpr (CACHED) {
+        const uint32_t span = block_span(jb, words);
+        use_table = span <= VBM_MAX_CACHED_LEAVES;
+        if (use_table) stage_leaf_table(g, fl, span, table);
+    }
+    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
+        const uint32_t index = 1u + b * W + s;
+        if (index > g.n) break;
+        const Slot d = decode_slot(g, fl, jb, s, index);
+        uint32_t* row = taps + (size_t)index * kBoxTaps;
+        if (CACHED && use_table) {
+            const TapResolver<true> resolve(g, table + (d.leaf - fl) * kBoxTaps, d);
+#pragma unroll
+            for (int t = 0; t < kBoxTaps; ++t) row[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
+        } else {
+            const TapResolver<false> resolve(g, nullptr, d);
+#pragma unroll
+            for (int t = 0; t < kBoxTaps; ++t) row[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
+        }
+    }
+    if (b == 0 && threadIdx.x < (unsigned)kBoxTaps) taps[threadIdx.x] = 0u;
+}
+
+template <int CC, bool VEC>
+cudaError_t launch_box_cc(const DevGrid& g, const float* sc, int C, int ch0, float* out, int resolver, int output,
+                          cudaStream_t stream) {
+    const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
+    const bool cached = resolver == VBM_RESOLVE_CACHED, mat = output == VBM_OUTPUT_MATERIALISED;
+    if (cached && mat) box_filter_kernel<CC, VEC, true, true><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else if (cached) box_filter_kernel<CC, VEC, true, false><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else if (mat) box_filter_kernel<CC, VEC, false, true><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else box_filter_kernel<CC, VEC, false, false><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_box_filter(const DevGrid& g, const float* sidecar, int C, float* out, int resolver, int output,
+                              cudaStream_t stream) {
+    if (g.n_blocks == 0) {
+        // Empty grid: only row 0 exists.
+        return cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, stream);
+    }
+    switch (C) {
+        case 1: return launch_box_cc<1, false>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 2: return launch_box_cc<2, false>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 3: return launch_box_cc<3, false>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 4: return launch_box_cc<4, true>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 8: return launch_box_cc<8, true>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 16: return launch_box_cc<16, true>(g, sidecar, C, 0, out, resolver, output, stream);
+        default: break;
+    }
+    // Other widths: chunks of 4 channels (scalar loads), then the remainder.
+    int ch0 = 0;
+    for (; ch0 + 4 <= C; ch0 += 4) {
+        cudaError_t e = launch_box_cc<4, false>(g, sidecar, C, ch0, out, resolver, output, stream);
+        if (e != cudaSuccess) return e;
+    }
+    switch (C - ch0) {
+        case 1: return launch_box_cc<1, false>(g, sidecar, C, ch0, out, resolver, output, stream);
+        case 2: return launch_box_cc<2, false>(g, sidecar, C, ch0, out, resolver, output, stream);
+        case 3: return launch_box_cc<3, false>(g, sidecar, C, ch0, out, resolver, output, stream);
+        default: return cudaSuccess;
+    }
+}
+
+cudaError_t launch_box_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream) {
+    if (g.n_blocks == 0) return cudaMemsetAsync(taps, 0, sizeof(uint32_t) * kBoxTaps, stream);
+    const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
+    if (resolver == VBM_RESOLVE_CACHED) box_taps_kernel<true><<<grid, block, 0, stream>>>(g, taps);
+    else box_taps_kernel<false><<<grid, block, 0, stream>>>(g, taps);
+    return cudaGetLastError();
+}
+
+}  // namespace vbm

@@ -1,0 +1,219 @@
+// 7-tap cross stencil (centre + six faces): Laplacian / 7-tap sum consumers
+// and the raw-tap export.
+//
+// Sources (web pages; cited by title and section):
+//   [2263] OpenVDB PR #2263 "Alternative stencil resolvers for VoxelBlockManager"
+//   [2258] OpenVDB PR #2258 "VBM select-based inverse-map decode"
+//
+// Taps j = 0..6 are the box taps t = 4, 10, 12, 13, 14, 16, 22, i.e. offsets
+// (-1,0,0), (0,-1,0), (0,0,-1), (0,0,0), (0,0,1), (0,1,0), (1,0,0).  The cross
+// resolvers materialise their 7 taps ([2263] "Notes": there is deliberately no
+// streaming cross resolver).  The cached form stages a 7-entry neighbour-leaf
+// row per spanned leaf (the pages' 16 x 7 table): entry j is the leaf holding
+// tap j's position when that position leaves the voxel's leaf, entry 3 the leaf
+// itself.  The 7-point Laplacian is named as a consumer in [2258] "A/B -
+// decode"; its formula here is s - 6*centre, s = the active face values summed
+// in increasing tap order, the product and the difference rounded separately.
+#include "vbm_device.cuh"
+#include "vbm_launch.h"
+
+namespace vbm {
+namespace {
+
+__device__ __forceinline__ constexpr int cross_di(int j) { return j == 0 ? -1 : j == 6 ? 1 : 0; }
+__device__ __forceinline__ constexpr int cross_dj(int j) { return j == 1 ? -1 : j == 5 ? 1 : 0; }
+__device__ __forceinline__ constexpr int cross_dk(int j) { return j == 2 ? -1 : j == 4 ? 1 : 0; }
+
+// Stage row[l*7 + j] for the block's spanned leaves; ends with a barrier.
+__device__ __forceinline__ void stage_cross_table(const DevGrid& g, uint32_t first_leaf, uint32_t span,
+                                                  uint32_t* __restrict__ table) {
+    for (uint32_t e = threadIdx.x; e < span * (uint32_t)kCrossTaps; e += blockDim.x) {
+        const uint32_t l = e / kCrossTaps, j = e - l * kCrossTaps;
+        const uint32_t L = first_leaf + l;
+        uint32_t id = L;
+        if (j != 3u) {
+            const LeafRec* rec = g.leaves + L;
+            id = find_leaf(g, __ldg(&rec->origin[0]) + 8 * cross_di((int)j), __ldg(&rec->origin[1]) + 8 * cross_dj((int)j),
+                           __ldg(&rec->origin[2]) + 8 * cross_dk((int)j));
+        }
+        table[e] = id;
+    }
+    __syncthreads();
+}
+
+// Resolve the 7 taps of one decoded voxel into st[].
+template <bool TABLE>
+__device__ __forceinline__ void resolve_cross(const DevGrid& g, const uint32_t* table_row, const Slot& d,
+                                              uint32_t (&st)[kCrossTaps]) {
+    const int32_t lx = (int32_t)(d.off >> 6), ly = (int32_t)((d.off >> 3) & 7u), lz = (int32_t)(d.off & 7u);
+    if constexpr (TABLE) {
+#pragma unroll
+        for (int j = 0; j < kCrossTaps; ++j) {
+            const int32_t nx = lx + cross_di(j), ny = ly + cross_dj(j), nz = lz + cross_dk(j);
+            const bool leaves_leaf = ((nx | ny | nz) & ~7) != 0;  // some coordinate is -1 or 8
+            const uint32_t NL = table_row[leaves_leaf ? j : 3];
+            st[j] = NL == kNone ? 0u : leaf_index_at(g.leaves, NL, pack_off(nx, ny, nz));
+        }
+    } else {
+        const LeafRec* r = g.leaves + d.leaf;
+        const int32_t x = __ldg(&r->origin[0]) + lx, y = __ldg(&r->origin[1]) + ly, z = __ldg(&r->origin[2]) + lz;
+#pragma unroll
+        for (int j = 0; j < kCrossTaps; ++j) st[j] = walk_index(g, x + cross_di(j), y + cross_dj(j), z + cross_dk(j));
+    }
+}
+
+template <int CC, bool VEC>
+__device__ __forceinline__ void load_row(float (&v)[CC], const float* __restrict__ sc, uint32_t idx, int C, int ch0) {
+    const float* row = sc + (size_t)idx * (size_t)C + ch0;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int q = 0; q < CC / 4; ++q) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(row) + q);
+            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int ch = 0; ch < CC; ++ch) v[ch] = __ldg(row + ch);
+    }
+}
+
+template <int CC, bool VEC, bool TABLE, int OP>
+__device__ __forceinline__ void cross_slot(const DevGrid& g, const uint32_t* table_row, const Slot& d, uint32_t index,
+                                           const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
+    uint32_t st[kCrossTaps];
+    resolve_cross<TABLE>(g, table_row, d, st);
+    float acc[CC], v[CC];
+#pragma unroll
+    for (int ch = 0; ch < CC; ++ch) acc[ch] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kCrossTaps; ++j) {
+        if (OP == VBM_CROSS_LAPLACIAN && j == 3) continue;  // the centre enters below
+        if (st[j]) {
+            load_row<CC, VEC>(v, sc, st[j], C, ch0);
+#pragma unroll
+            for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], v[ch]);
+        }
+    }
+    if constexpr (OP == VBM_CROSS_LAPLACIAN) {
+        load_row<CC, VEC>(v, sc, index, C, ch0);
+#pragma unroll
+        for (int ch = 0; ch < CC; ++ch) acc[ch] = __fsub_rn(acc[ch], __fmul_rn(6.0f, v[ch]));
+    }
+    float* row = out + (size_t)index * (size_t)C + ch0;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int q = 0; q < CC / 4; ++q)
+            reinterpret_cast<float4*>(row)[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int ch = 0; ch < CC; ++ch) row[ch] = acc[ch];
+    }
+}
+
+template <int CC, bool VEC, bool CACHED, int OP>
+__global__ void __launch_bounds__(512) cross_filter_kernel(DevGrid g, const float* __restrict__ sc,
+                                                           float* __restrict__ out, int C, int ch0) {
+    __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kCrossTaps : 1];
+    const uint32_t W = 1u << g.log2w, words = W >> 6;
+    const uint32_t b = blockIdx.x;
+    const uint64_t* jb = g.jump + (size_t)b * words;
+    const uint32_t fl = __ldg(&g.first_leaf[b]);
+    bool use_table = false;
+    if constexpr (CACHED) {
+        const uint32_t span = block_span(jb, words);
+        use_table = span <= VBM_MAX_CACHED_LEAVES;
+        if (use_table) stage_cross_table(g, fl, span, table);
+    }
+    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
+        const uint32_t index = 1u + b * W + s;
+        if (index > g.n) break;
+        const Slot d = decode_slot(g, fl, jb, s, index);
+        if constexpr (CACHED) {
+            if (use_table) {
+                cross_slot<CC, VEC, true, OP>(g, table + (d.leaf - fl) * kCrossTaps, d, index, sc, out, C, ch0);
+                continue;
+            }
+        }
+        cross_slot<CC, VEC, false, OP>(g, nullptr, d, index, sc, out, C, ch0);
+    }
+    if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
+}
+
+template <bool CACHED>
+__global__ void __launch_bounds__(512) cross_taps_kernel(DevGrid g, uint32_t* __restrict__ taps) {
+    __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kCrossTaps : 1];
+    const uint32_t W = 1u << g.log2w, words = W >> 6;
+    const uint32_t b = blockIdx.x;
+    const uint64_t* jb = g.jump + (size_t)b * words;
+    const uint32_t fl = __ldg(&g.first_leaf[b]);
+    bool use_table = false;
+    if constexpr (CACHED) {
+        const uint32_t span = block_span(jb, words);
+        use_table = span <= VBM_MAX_CACHED_LEAVES;
+        if (use_table) stage_cross_table(g, fl, span, table);
+    }
+    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
+        const uint32_t index = 1u + b * W + s;
+        if (index > g.n) break;
+        const Slot d = decode_slot(g, fl, jb, s, index);
+        uint32_t st[kCrossTaps];
+        if (CACHED && use_table) resolve_cross<true>(g, table + (d.leaf - fl) * kCrossTaps, d, st);
+        else resolve_cross<false>(g, nullptr, d, st);
+        uint32_t* row = taps + (size_t)index * kCrossTaps;
+#pragma unroll
+        for (int j = 0; j < kCrossTaps; ++j) row[j] = st[j];
+    }
+    if (b == 0 && threadIdx.x < (unsigned)kCrossTaps) taps[threadIdx.x] = 0u;
+}
+
+template <int CC, bool VEC>
+cudaError_t launch_cross_cc(const DevGrid& g, const float* sc, int C, int ch0, float* out, int resolver, int op,
+                            cudaStream_t stream) {
+    const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
+    const bool cached = resolver == VBM_RESOLVE_CACHED;
+    if (op == VBM_CROSS_LAPLACIAN) {
+        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_LAPLACIAN><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_LAPLACIAN><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    } else {
+        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_SUM><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_SUM><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cross_filter(const DevGrid& g, const float* sidecar, int C, float* out, int resolver, int op,
+                                cudaStream_t stream) {
+    if (g.n_blocks == 0) return cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, stream);
+    switch (C) {
+        case 1: return launch_cross_cc<1, false>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 2: return launch_cross_cc<2, false>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 3: return launch_cross_cc<3, false>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 4: return launch_cross_cc<4, true>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 8: return launch_cross_cc<8, true>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 16: return launch_cross_cc<16, true>(g, sidecar, C, 0, out, resolver, op, stream);
+        default: break;
+    }
+    int ch0 = 0;
+    for (; ch0 + 4 <= C; ch0 += 4) {
+        cudaError_t e = launch_cross_cc<4, false>(g, sidecar, C, ch0, out, resolver, op, stream);
+        if (e != cudaSuccess) return e;
+    }
+    switch (C - ch0) {
+        case 1: return launch_cross_cc<1, false>(g, sidecar, C, ch0, out, resolver, op, stream);
+        case 2: return launch_cross_cc<2, false>(g, sidecar, C, ch0, out, resolver, op, stream);
+        case 3: return launch_cross_cc<3, false>(g, sidecar, C, ch0, out, resolver, op, stream);
+        default: return cudaSuccess;
+    }
+}
+
+cudaError_t launch_cross_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream) {
+    if (g.n_blocks == 0) return cudaMemsetAsync(taps, 0, sizeof(uint32_t) * kCrossTaps, stream);
+    const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
+    if (resolver == VBM_RESOLVE_CACHED) cross_taps_kernel<true><<<grid, block, 0, stream>>>(g, taps);
+    else cross_taps_kernel<false><<<grid, block, 0, stream>>>(g, taps);
+    return cudaGetLastError();
+}
+
+}  // namespace vbm

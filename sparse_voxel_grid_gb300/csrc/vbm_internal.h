@@ -1,0 +1,97 @@
+// Internal layout of a vbm_grid: host-side arrays written by the builder and
+// the device arena the kernels read.  Shared by the builder (vbm_build.cpp),
+// the C ABI (vbm_api.cu) and the kernels; not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/vbm.h"
+
+#ifdef __CUDACC__
+#define VBM_HD __host__ __device__ __forceinline__
+#else
+#define VBM_HD inline
+#endif
+
+namespace vbm {
+
+constexpr uint32_t kNone = 0xFFFFFFFFu;     // absent child / leaf / sentinel leaf index
+constexpr uint16_t kNoOffset = 0xFFFF;      // sentinel voxel offset
+constexpr int kUpperSlots = 32 * 32 * 32;   // children of an upper node (lower nodes)
+constexpr int kLowerSlots = 16 * 16 * 16;   // children of a lower node (leaves)
+constexpr int kBoxTaps = 27;
+constexpr int kCrossTaps = 7;
+constexpr int kMaxC = 64;
+
+// One leaf: 128 bytes, one cache line.  `mask` is the 512-bit value mask (bit
+// off%64 of word off/64, off = x*64 + y*8 + z in-leaf); `prefix` is the 9-bit
+// directory the decode reads (field w-1, w = 1..7, at bits 9(w-1)..9w-1 = set
+// bits in words 0..w-1); `base[w]` = first + prefix(w) is the same directory
+// pre-added to the first index, which the resolvers use to rank a bit with one
+// popcount.
+struct alignas(128) LeafRec {
+    uint64_t mask[8];   // bytes 0..63
+    uint32_t base[8];   // bytes 64..95
+    uint64_t prefix;    // bytes 96..103
+    uint32_t first;     // bytes 104..107: index of the first active voxel
+    int32_t origin[3];  // bytes 108..119
+    uint32_t count;     // bytes 120..123: active voxels in the leaf
+    uint32_t pad;
+};
+static_assert(sizeof(LeafRec) == 128, "LeafRec must be one 128-byte line");
+
+// Root key of the upper node containing (x,y,z): the signed upper-node
+// coordinates (x>>12, y>>12, z>>12) biased by 2^19 into 20 bits each, so that
+// unsigned order of keys is signed lexicographic order of the upper origins.
+VBM_HD uint64_t root_key_of(int32_t x, int32_t y, int32_t z) {
+    return ((uint64_t)(uint32_t)((x >> 12) + (1 << 19)) << 40) | ((uint64_t)(uint32_t)((y >> 12) + (1 << 19)) << 20) |
+           (uint64_t)(uint32_t)((z >> 12) + (1 << 19));
+}
+
+// Everything a kernel needs, passed by value.
+struct DevGrid {
+    const LeafRec* leaves;
+    const uint64_t* root_keys;   // n_upper sorted keys
+    const uint32_t* upper;       // n_upper x 32768: lower-node id or kNone
+    const uint32_t* lower;       // n_lower x 4096: leaf id or kNone
+    const uint32_t* first_leaf;  // n_blocks
+    const uint64_t* jump;        // n_blocks x (W/64)
+    uint32_t n;                  // active voxels
+    uint32_t n_leaves;
+    uint32_t n_blocks;
+    uint32_t n_upper;
+    int log2w;
+};
+
+}  // namespace vbm
+
+struct vbm_grid {
+    // sizes
+    uint64_t n = 0;
+    int log2w = 7;
+    uint32_t n_upper = 0, n_lower = 0;
+    uint64_t n_leaves = 0, n_blocks = 0;
+    uint64_t n_over_cache = 0;
+    uint32_t max_span = 0;
+    // host arrays
+    std::vector<vbm::LeafRec> leaves;
+    std::vector<uint64_t> root_keys;
+    std::vector<uint32_t> upper;
+    std::vector<uint32_t> lower;
+    std::vector<uint32_t> first_leaf;
+    std::vector<uint64_t> jump;
+    // device arena (one allocation) and the views into it
+    void* arena = nullptr;
+    size_t arena_bytes = 0;
+    int device = -1;
+    vbm::DevGrid dev{};
+};
+
+namespace vbm {
+// Host builder (vbm_build.cpp).  Fills every host array of g; returns a status
+// code and sets err on failure.
+int build_host(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, vbm_grid* g, std::string& err);
+}  // namespace vbm

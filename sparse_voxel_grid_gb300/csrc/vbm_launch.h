@@ -1,0 +1,25 @@
+// Kernel launchers called by the C ABI (vbm_api.cu).  Each enqueues work on
+// `stream` and returns the launch status; arguments are validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "vbm_internal.h"
+
+namespace vbm {
+
+cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream);
+
+cudaError_t launch_box_filter(const DevGrid& g, const float* sidecar, int C, float* out, int resolver, int output,
+                              cudaStream_t stream);
+
+cudaError_t launch_cross_filter(const DevGrid& g, const float* sidecar, int C, float* out, int resolver, int op,
+                                cudaStream_t stream);
+
+cudaError_t launch_box_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream);
+cudaError_t launch_cross_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream);
+
+// Threads per block for a block width of 2^log2w slots (one slot per thread).
+inline int threads_for(int log2w) { return 1 << log2w; }
+
+}  // namespace vbm

@@ -1,0 +1,63 @@
+"""Helpers for the GPU parity tests: run the library's calls through the
+Python binding (which calls the C ABI) and bring results back as numpy."""
+from __future__ import annotations
+
+import numpy as np
+
+import sparse_voxel_grid_gb300 as vbm
+
+
+def torch():
+    import torch as t
+    return t
+
+
+def require_gpu():
+    import pytest
+    t = torch()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    vbm.load()
+
+
+def to_dev(a: np.ndarray):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def decode(g):
+    t = torch()
+    m = g.n_slots
+    li = t.empty(m, dtype=t.int32, device="cuda")
+    vo = t.empty(m, dtype=t.int16, device="cuda")
+    vbm.vbm_decode(g, li, vo)
+    t.cuda.synchronize()
+    return li.cpu().numpy().view(np.uint32), vo.cpu().numpy().view(np.uint16)
+
+
+def box_filter(g, sidecar_dev, C, resolver, output):
+    t = torch()
+    out = t.full(((g.n + 1) * C,), float("nan"), dtype=t.float32, device="cuda")
+    vbm.vbm_box_filter(g, sidecar_dev, C, out, resolver, output)
+    t.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def cross_filter(g, sidecar_dev, C, resolver, op):
+    t = torch()
+    out = t.full(((g.n + 1) * C,), float("nan"), dtype=t.float32, device="cuda")
+    vbm.vbm_cross_filter(g, sidecar_dev, C, out, resolver, op)
+    t.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def taps(g, shape, resolver):
+    t = torch()
+    out = t.full(((g.n + 1) * shape,), -1, dtype=t.int32, device="cuda")
+    (vbm.vbm_box_taps if shape == 27 else vbm.vbm_cross_taps)(g, out, resolver)
+    t.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint32).reshape(-1, shape)
+
+
+def bits(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float32).view(np.uint32)

@@ -1,0 +1,143 @@
+"""GPU parity on small grids: every output element of the CUDA path (through
+the C ABI) against the CPU oracle, bit for bit.
+
+Grids span several VBM blocks and end in a ragged last block; they include
+negative coordinates, upper/lower-node boundaries, blocks that overflow the
+cached table (one voxel per leaf), and degenerate sizes.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import sparse_voxel_grid_gb300 as vbm
+import synth
+from tests import gpu_util as gu
+from tests.test_oracle_pins import GRIDS
+
+pytestmark = pytest.mark.gpu
+
+
+def _single():
+    return np.array([[-3, 7, 12]], dtype=np.int32)
+
+
+def _exact_blocks(n=256):
+    # exactly two blocks of 128 (no partial block) from a dense slab
+    c = synth.dense_random((8, 8, 16), 1.0, origin=(0, -4, 0))
+    return c[:n]
+
+
+SMALL = dict(GRIDS)
+SMALL.update({
+    "scatter": lambda: synth.scatter(side=10, count=700, origin=-37, seed=5),
+    "single": _single,
+    "exact_blocks": _exact_blocks,
+    "exact_plus_one": lambda: _exact_blocks(257),
+})
+
+RESOLVERS = [vbm.RESOLVE_TREEWALK, vbm.RESOLVE_CACHED]
+OUTPUTS = [vbm.OUTPUT_STREAMED, vbm.OUTPUT_MATERIALISED]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    gu.require_gpu()
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def case(request):
+    coords = SMALL[request.param]()
+    return request.param, coords, oracle.OracleGrid(coords)
+
+
+@pytest.mark.parametrize("log2w", [6, 7, 8, 9])
+def test_decode(case, log2w):
+    _, coords, o = case
+    g = vbm.vbm_build(coords, log2w)
+    li, vo = gu.decode(g)
+    wli, wvo = o.decode(log2w)
+    np.testing.assert_array_equal(li, wli)
+    np.testing.assert_array_equal(vo, wvo)
+
+
+@pytest.mark.parametrize("log2w", [7, 9])
+@pytest.mark.parametrize("resolver", RESOLVERS)
+def test_taps(case, log2w, resolver):
+    _, coords, o = case
+    g = vbm.vbm_build(coords, log2w)
+    np.testing.assert_array_equal(gu.taps(g, 27, resolver), o.taps(27))
+    np.testing.assert_array_equal(gu.taps(g, 7, resolver), o.taps(7))
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 4, 5, 8, 13, 16])
+def test_box_filter_all_variants(case, C):
+    _, coords, o = case
+    s = synth.sidecar_uniform(o.n, C, seed=C)
+    want = gu.bits(o.box_filter(s, C))
+    sd = gu.to_dev(s)
+    for log2w in (6, 7, 9):
+        g = vbm.vbm_build(coords, log2w)
+        for r in RESOLVERS:
+            for out in OUTPUTS:
+                got = gu.bits(gu.box_filter(g, sd, C, r, out))
+                np.testing.assert_array_equal(got, want, err_msg=f"W=2^{log2w} resolver={r} output={out}")
+
+
+@pytest.mark.parametrize("C", [1, 3, 8, 16])
+@pytest.mark.parametrize("op", [vbm.CROSS_LAPLACIAN, vbm.CROSS_SUM])
+def test_cross_filter(case, C, op):
+    _, coords, o = case
+    s = synth.sidecar_uniform(o.n, C, seed=100 + C)
+    want = gu.bits(o.cross_filter(s, C, op=op))
+    sd = gu.to_dev(s)
+    for log2w in (6, 8):
+        g = vbm.vbm_build(coords, log2w)
+        for r in RESOLVERS:
+            got = gu.bits(gu.cross_filter(g, sd, C, r, op))
+            np.testing.assert_array_equal(got, want, err_msg=f"W=2^{log2w} resolver={r}")
+
+
+def test_constant_sidecar_counts():
+    coords = SMALL["tiny_shell"]()
+    o = oracle.OracleGrid(coords)
+    g = vbm.vbm_build(coords, 7)
+    one = np.ones(o.n + 1, dtype=np.float32)
+    one[0] = 0
+    got = gu.box_filter(g, gu.to_dev(one), 1, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED)
+    np.testing.assert_array_equal(got, o.box_filter(one, 1))
+    assert got[0] == 0 and got[1:].min() >= 1 and got[1:].max() <= 27
+
+
+def test_empty_grid():
+    t = gu.torch()
+    g = vbm.vbm_build(np.zeros((0, 3), dtype=np.int32), 7)
+    assert g.n == 0 and g.n_slots == 0
+    s = t.zeros(3, device="cuda")
+    out = t.full((3,), 5.0, device="cuda")
+    vbm.vbm_box_filter(g, s, 3, out)
+    vbm.vbm_cross_filter(g, s, 3, out)
+    taps = t.full((27,), 9, dtype=t.int32, device="cuda")
+    vbm.vbm_box_taps(g, taps)
+    t.cuda.synchronize()
+    assert (out.cpu() == 0).all() and (taps.cpu() == 0).all()
+
+
+def test_device_errors():
+    t = gu.torch()
+    coords = SMALL["tiny_shell"]()
+    g = vbm.vbm_build(coords, 7)
+    n = g.n
+    buf = t.zeros(n + 2, dtype=t.float32, device="cuda")
+    lib = vbm.load()
+    import ctypes
+    buf2 = t.zeros(n + 2, dtype=t.float32, device="cuda")
+    mis = ctypes.c_void_p(buf.data_ptr() + 4)
+    ok = ctypes.c_void_p(buf.data_ptr())
+    ok2 = ctypes.c_void_p(buf2.data_ptr())
+    assert lib.vbm_box_filter(g.handle, mis, 1, ok, 1, 0, None) == -6
+    assert lib.vbm_box_filter(g.handle, ok, 0, ok, 1, 0, None) == -1
+    assert lib.vbm_box_filter(g.handle, ok, 65, ok, 1, 0, None) == -1
+    assert lib.vbm_box_filter(g.handle, ok, 1, ok, 1, 0, None) == -1  # aliasing
+    assert lib.vbm_box_filter(g.handle, ok, 1, mis, 7, 0, None) == -1
+    assert lib.vbm_cross_filter(g.handle, ok, 1, ok2, 1, 5, None) == -1
+    assert b"op" in lib.vbm_last_error()
