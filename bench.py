@@ -132,7 +132,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     coords = synth.WORKLOADS["S185"]()
-    g = vbm.vbm_build(coords, LOG2W)
+    g = vbm.vbm_build(coords, args.log2w)
     info = g.info
     n, W = info["n_active"], info["block_width"]
     stream = torch.cuda.current_stream()
@@ -142,7 +142,9 @@ def run_gpu(args):
     sidecars = {C: torch.from_numpy(synth.sidecar_uniform(n, C, seed=0)).cuda() for C in CS}
     outs = {C: torch.empty_like(sidecars[C]) for C in CS}
 
-    def launch(C, resolver=vbm.RESOLVE_CACHED, output=vbm.OUTPUT_STREAMED, grid=g):
+    resolver = {"cached": vbm.RESOLVE_CACHED, "brick": vbm.RESOLVE_BRICK, "walk": vbm.RESOLVE_TREEWALK}[args.resolver]
+
+    def launch(C, output=vbm.OUTPUT_STREAMED, grid=g):
         vbm.vbm_box_filter(grid, sidecars[C], C, outs[C], resolver, output, stream)
 
     def timed_launch(fn):
@@ -196,12 +198,12 @@ def run_gpu(args):
     dom_ms = statistics.mean(per_c_ms[dom])
     dom_bytes = algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, dom)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = load_traffic(f"box_cached_streamed_C{dom}")
+    traffic = load_traffic(f"box_{args.resolver}_W{W}_C{dom}")
 
     # end to end through the public API: pinned host sidecar -> device -> filter -> host
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(torch, vbm, g, n, sidecars, outs, args, stream)
+        e2e = run_e2e(torch, vbm, g, n, sidecars, outs, args, stream, resolver)
 
     variants = run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args) if not args.no_variants else None
     cpu = None
@@ -213,14 +215,14 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": f"{WORKLOAD}, N={n}, leaves={info['n_leaves']}, fused decode + cached resolver + "
-                               f"streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
+        "config": {"workload": f"{WORKLOAD}, N={n}, leaves={info['n_leaves']}, fused decode + {args.resolver} "
+                               f"resolver + streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
                    "n_active": n, "n_leaves": info["n_leaves"], "block_width": W, "channels": list(CS),
-                   "resolver": "cached", "output": "streamed", "l2": "flushed before every launch",
+                   "resolver": args.resolver, "output": "streamed", "l2": "flushed before every launch",
                    "value_counts": "4*N voxels per step (one per channel width)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
-        "roofline": {"bound": "hbm", "kernel": f"box_filter cached streamed C={dom}", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": f"box filter ({args.resolver} resolver, streamed) C={dom}", "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes},
@@ -247,7 +249,7 @@ def load_traffic(key):
     return d.get(key)
 
 
-def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream):
+def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream, resolver):
     host_in = {C: sidecars[C].cpu().pin_memory() for C in CS}
     host_out = {C: torch.empty_like(host_in[C]).pin_memory() for C in CS}
     dev_in = {C: torch.empty_like(sidecars[C]) for C in CS}
@@ -255,7 +257,7 @@ def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream):
     def step():
         for C in CS:
             dev_in[C].copy_(host_in[C], non_blocking=True)
-            vbm.vbm_box_filter(g, dev_in[C], C, outs[C], vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED, stream)
+            vbm.vbm_box_filter(g, dev_in[C], C, outs[C], resolver, vbm.OUTPUT_STREAMED, stream)
             host_out[C].copy_(outs[C], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -291,15 +293,18 @@ def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
     for log2w in (7, 9):
         g = vbm.vbm_build(coords, log2w)
         for C in CS:
-            for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED)):
-                for oname, o in (("streamed", vbm.OUTPUT_STREAMED), ("materialised", vbm.OUTPUT_MATERIALISED)):
+            for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED),
+                             ("brick", vbm.RESOLVE_BRICK)):
+                outputs = (("streamed", vbm.OUTPUT_STREAMED), ("materialised", vbm.OUTPUT_MATERIALISED))
+                for oname, o in (outputs if r != vbm.RESOLVE_BRICK else outputs[:1]):
                     ms = tmean(lambda: vbm.vbm_box_filter(g, sidecars[C], C, outs[C], r, o))
                     res.append({"kernel": "box", "W": 1 << log2w, "C": C, "resolver": rname, "output": oname,
                                 "ms": round(ms, 5)})
         g.close()
     for log2w in (6, 7, 8, 9):
         g = vbm.vbm_build(coords, log2w)
-        for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED)):
+        for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED),
+                         ("brick", vbm.RESOLVE_BRICK)):
             ms = tmean(lambda: vbm.vbm_cross_filter(g, sidecars[1], 1, outs[1], r, vbm.CROSS_LAPLACIAN))
             res.append({"kernel": "laplacian", "W": 1 << log2w, "C": 1, "resolver": rname, "ms": round(ms, 5)})
         li = torch.empty(g.n_slots, dtype=torch.int32, device="cuda")
@@ -384,6 +389,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--resolver", choices=["cached", "brick", "walk"], default="cached")
+    ap.add_argument("--log2w", type=int, default=LOG2W, choices=[6, 7, 8, 9])
     ap.add_argument("--cpu-sample", type=int, default=150000)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--variant-reps", type=int, default=5)

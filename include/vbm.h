@@ -69,6 +69,8 @@ extern "C" {
 /* resolver: how a tap's index is found ([2263] "Summary" table) */
 #define VBM_RESOLVE_TREEWALK 0 /* root-down tree traversal per tap; no shared memory */
 #define VBM_RESOLVE_CACHED 1   /* per-block neighbour-leaf table staged in shared memory */
+#define VBM_RESOLVE_BRICK 2    /* cached table + per-leaf padded index/value brick in shared memory
+                                  (this library's GB300 resolver; no counterpart on the pages) */
 
 /* output: how taps reach the consumer ([2262] "Summary", [2263] "Summary") */
 #define VBM_OUTPUT_STREAMED 0     /* each (tap, index) consumed as it is resolved (forEach*) */
@@ -148,7 +150,13 @@ int vbm_decode(const vbm_grid* grid, uint32_t* leaf_index, uint16_t* voxel_offse
  * reassociation), so every resolver/output combination gives the same bits.
  * Each slot is decoded in registers, its taps resolved by `resolver`
  * (VBM_RESOLVE_*) and consumed per `output` (VBM_OUTPUT_*); blocks spanning more
- * than VBM_MAX_CACHED_LEAVES leaves use the tree walk.  sidecar and out are
+ * than VBM_MAX_CACHED_LEAVES leaves use the tree walk.  VBM_RESOLVE_BRICK
+ * stages, for each leaf the block spans, a 10x10x10 brick of the leaf and its
+ * one-voxel halo in shared memory (indices ranked once per brick row, then the
+ * sidecar values), so each tap is one shared-memory read; it adds +0.0 for
+ * inactive taps, which leaves an fp32 sum that started at +0.0 unchanged bit for
+ * bit, so all resolvers agree.  `output` does not apply to it (must be
+ * VBM_OUTPUT_STREAMED or VBM_OUTPUT_MATERIALISED; both run the same kernel).  sidecar and out are
  * device arrays of (N+1)*C floats.  Errors: INVALID, STATE, ALIGN, CUDA. */
 int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out, int resolver, int output,
                    void* stream);

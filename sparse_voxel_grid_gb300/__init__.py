@@ -23,6 +23,7 @@ BUILD_DEDUP = _K["VBM_BUILD_DEDUP"]
 BUILD_HOST_ONLY = _K["VBM_BUILD_HOST_ONLY"]
 RESOLVE_TREEWALK = _K["VBM_RESOLVE_TREEWALK"]
 RESOLVE_CACHED = _K["VBM_RESOLVE_CACHED"]
+RESOLVE_BRICK = _K["VBM_RESOLVE_BRICK"]
 OUTPUT_STREAMED = _K["VBM_OUTPUT_STREAMED"]
 OUTPUT_MATERIALISED = _K["VBM_OUTPUT_MATERIALISED"]
 CROSS_LAPLACIAN = _K["VBM_CROSS_LAPLACIAN"]

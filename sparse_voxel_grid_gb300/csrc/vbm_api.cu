@@ -234,7 +234,7 @@ static int check_filter(const vbm_grid* g, const float* sidecar, int C, const fl
     int rc = check_grid(g, fn);
     if (rc) return rc;
     if (C < 1 || C > vbm::kMaxC) return fail(VBM_ERR_INVALID, std::string(fn) + ": C must be in 1..64");
-    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED)
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED && resolver != VBM_RESOLVE_BRICK)
         return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
     if ((rc = check_ptr(sidecar, fn, "sidecar"))) return rc;
     if ((rc = check_ptr(out, fn, "out"))) return rc;
@@ -251,7 +251,11 @@ int vbm_box_filter(const vbm_grid* g, const float* sidecar, int C, float* out, i
         return fail(VBM_ERR_INVALID, "vbm_box_filter: unknown output mode");
     DeviceGuard guard(g->device);
     if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_box_filter: cannot select the grid's device");
-    cudaError_t e = vbm::launch_box_filter(g->dev, sidecar, C, out, resolver, output, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (g->n_blocks == 0) e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, s);
+    else if (resolver == VBM_RESOLVE_BRICK) e = vbm::launch_brick_box(g->dev, sidecar, C, out, s);
+    else e = vbm::launch_box_filter(g->dev, sidecar, C, out, resolver, output, s);
     return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter: launch", e);
 }
 
@@ -264,7 +268,11 @@ int vbm_cross_filter(const vbm_grid* g, const float* sidecar, int C, float* out,
         return fail(VBM_ERR_INVALID, "vbm_cross_filter: unknown op");
     DeviceGuard guard(g->device);
     if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_cross_filter: cannot select the grid's device");
-    cudaError_t e = vbm::launch_cross_filter(g->dev, sidecar, C, out, resolver, op, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (g->n_blocks == 0) e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, s);
+    else if (resolver == VBM_RESOLVE_BRICK) e = vbm::launch_brick_cross(g->dev, sidecar, C, out, op, s);
+    else e = vbm::launch_cross_filter(g->dev, sidecar, C, out, resolver, op, s);
     return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_cross_filter: launch", e);
 }
 
@@ -272,13 +280,16 @@ static int taps_common(const vbm_grid* g, uint32_t* taps, int resolver, void* st
     const char* fn = box ? "vbm_box_taps" : "vbm_cross_taps";
     int rc = check_grid(g, fn);
     if (rc) return rc;
-    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED)
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED && resolver != VBM_RESOLVE_BRICK)
         return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
     if ((rc = check_ptr(taps, fn, "taps"))) return rc;
     DeviceGuard guard(g->device);
     if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = box ? vbm::launch_box_taps(g->dev, taps, resolver, s) : vbm::launch_cross_taps(g->dev, taps, resolver, s);
+    cudaError_t e;
+    if (g->n_blocks == 0) e = cudaMemsetAsync(taps, 0, sizeof(uint32_t) * (box ? vbm::kBoxTaps : vbm::kCrossTaps), s);
+    else if (resolver == VBM_RESOLVE_BRICK) e = vbm::launch_brick_taps(g->dev, taps, box ? vbm::kBoxTaps : vbm::kCrossTaps, s);
+    else e = box ? vbm::launch_box_taps(g->dev, taps, resolver, s) : vbm::launch_cross_taps(g->dev, taps, resolver, s);
     return e == cudaSuccess ? VBM_OK : fail_cuda((std::string(fn) + ": launch").c_str(), e);
 }
 

@@ -14,97 +14,11 @@
 // materialised: all 27 indices are resolved into a per-thread array first
 // (computeBoxStencil).  Both add the same values in the same order, so the
 // results are identical bit for bit ([2262] "Validation").
-#include "vbm_device.cuh"
 #include "vbm_launch.h"
+#include "vbm_stencil.cuh"
 
 namespace vbm {
 namespace {
-
-// acc[ch] += sidecar[idx*C + ch0 + ch] for ch < CC; VEC: the row is read as
-// float4s (CC % 4 == 0 and rows 16-byte aligned).
-template <int CC, bool VEC>
-__device__ __forceinline__ void gather_add(float (&acc)[CC], const float* __restrict__ sc, uint32_t idx, int C,
-                                           int ch0) {
-    const float* row = sc + (size_t)idx * (size_t)C + ch0;
-    if constexpr (VEC) {
-#pragma unroll
-        for (int q = 0; q < CC / 4; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
-            acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], v.x);
-            acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], v.y);
-            acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
-            acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], v.w);
-        }
-    } else {
-#pragma unroll
-        for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], __ldg(row + ch));
-    }
-}
-
-template <int CC, bool VEC>
-__device__ __forceinline__ void store_row(float* __restrict__ out, uint32_t index, int C, int ch0,
-                                          const float (&acc)[CC]) {
-    float* row = out + (size_t)index * (size_t)C + ch0;
-    if constexpr (VEC) {
-#pragma unroll
-        for (int q = 0; q < CC / 4; ++q)
-            reinterpret_cast<float4*>(row)[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-    } else {
-#pragma unroll
-        for (int ch = 0; ch < CC; ++ch) row[ch] = acc[ch];
-    }
-}
-
-// Resolves tap (di,dj,dk) of one decoded voxel.  TABLE: through the block's
-// staged neighbour-leaf table row of the voxel's leaf; otherwise by tree walk.
-template <bool TABLE>
-struct TapResolver {
-    const DevGrid* g;
-    const uint32_t* row;     // TABLE: 27 neighbour-leaf ids of the voxel's leaf
-    int32_t x, y, z;         // TABLE: in-leaf position (0..7); walk: absolute coordinate
-
-    __device__ __forceinline__ TapResolver(const DevGrid& grid, const uint32_t* table_row, const Slot& d) : g(&grid) {
-        const int32_t lx = (int32_t)(d.off >> 6), ly = (int32_t)((d.off >> 3) & 7u), lz = (int32_t)(d.off & 7u);
-        if constexpr (TABLE) {
-            row = table_row;
-            x = lx; y = ly; z = lz;
-        } else {
-            row = nullptr;
-            const LeafRec* r = grid.leaves + d.leaf;
-            x = __ldg(&r->origin[0]) + lx;
-            y = __ldg(&r->origin[1]) + ly;
-            z = __ldg(&r->origin[2]) + lz;
-        }
-    }
-    __device__ __forceinline__ uint32_t operator()(int di, int dj, int dk) const {
-        if constexpr (TABLE) return cached_index(g->leaves, row, x + di, y + dj, z + dk);
-        else return walk_index(*g, x + di, y + dj, z + dk);
-    }
-};
-
-template <int CC, bool VEC, bool TABLE, bool MAT>
-__device__ __forceinline__ void box_slot(const DevGrid& g, const uint32_t* table_row, const Slot& d, uint32_t index,
-                                         const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
-    const TapResolver<TABLE> resolve(g, table_row, d);
-    float acc[CC];
-#pragma unroll
-    for (int ch = 0; ch < CC; ++ch) acc[ch] = 0.0f;
-    if constexpr (MAT) {
-        uint32_t st[kBoxTaps];
-#pragma unroll
-        for (int t = 0; t < kBoxTaps; ++t) st[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
-#pragma unroll
-        for (int t = 0; t < kBoxTaps; ++t)
-            if (st[t]) gather_add<CC, VEC>(acc, sc, st[t], C, ch0);
-    } else {
-#pragma unroll
-        for (int t = 0; t < kBoxTaps; ++t) {
-            const uint32_t idx = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
-            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
-        }
-    }
-    store_row<CC, VEC>(out, index, C, ch0, acc);
-}
 
 template <int CC, bool VEC, bool CACHED, bool MAT>
 __global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float* __restrict__ sc,

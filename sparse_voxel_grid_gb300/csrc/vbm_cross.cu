@@ -14,101 +14,11 @@
 // itself.  The 7-point Laplacian is named as a consumer in [2258] "A/B -
 // decode"; its formula here is s - 6*centre, s = the active face values summed
 // in increasing tap order, the product and the difference rounded separately.
-#include "vbm_device.cuh"
 #include "vbm_launch.h"
+#include "vbm_stencil.cuh"
 
 namespace vbm {
 namespace {
-
-__device__ __forceinline__ constexpr int cross_di(int j) { return j == 0 ? -1 : j == 6 ? 1 : 0; }
-__device__ __forceinline__ constexpr int cross_dj(int j) { return j == 1 ? -1 : j == 5 ? 1 : 0; }
-__device__ __forceinline__ constexpr int cross_dk(int j) { return j == 2 ? -1 : j == 4 ? 1 : 0; }
-
-// Stage row[l*7 + j] for the block's spanned leaves; ends with a barrier.
-__device__ __forceinline__ void stage_cross_table(const DevGrid& g, uint32_t first_leaf, uint32_t span,
-                                                  uint32_t* __restrict__ table) {
-    for (uint32_t e = threadIdx.x; e < span * (uint32_t)kCrossTaps; e += blockDim.x) {
-        const uint32_t l = e / kCrossTaps, j = e - l * kCrossTaps;
-        const uint32_t L = first_leaf + l;
-        uint32_t id = L;
-        if (j != 3u) {
-            const LeafRec* rec = g.leaves + L;
-            id = find_leaf(g, __ldg(&rec->origin[0]) + 8 * cross_di((int)j), __ldg(&rec->origin[1]) + 8 * cross_dj((int)j),
-                           __ldg(&rec->origin[2]) + 8 * cross_dk((int)j));
-        }
-        table[e] = id;
-    }
-    __syncthreads();
-}
-
-// Resolve the 7 taps of one decoded voxel into st[].
-template <bool TABLE>
-__device__ __forceinline__ void resolve_cross(const DevGrid& g, const uint32_t* table_row, const Slot& d,
-                                              uint32_t (&st)[kCrossTaps]) {
-    const int32_t lx = (int32_t)(d.off >> 6), ly = (int32_t)((d.off >> 3) & 7u), lz = (int32_t)(d.off & 7u);
-    if constexpr (TABLE) {
-#pragma unroll
-        for (int j = 0; j < kCrossTaps; ++j) {
-            const int32_t nx = lx + cross_di(j), ny = ly + cross_dj(j), nz = lz + cross_dk(j);
-            const bool leaves_leaf = ((nx | ny | nz) & ~7) != 0;  // some coordinate is -1 or 8
-            const uint32_t NL = table_row[leaves_leaf ? j : 3];
-            st[j] = NL == kNone ? 0u : leaf_index_at(g.leaves, NL, pack_off(nx, ny, nz));
-        }
-    } else {
-        const LeafRec* r = g.leaves + d.leaf;
-        const int32_t x = __ldg(&r->origin[0]) + lx, y = __ldg(&r->origin[1]) + ly, z = __ldg(&r->origin[2]) + lz;
-#pragma unroll
-        for (int j = 0; j < kCrossTaps; ++j) st[j] = walk_index(g, x + cross_di(j), y + cross_dj(j), z + cross_dk(j));
-    }
-}
-
-template <int CC, bool VEC>
-__device__ __forceinline__ void load_row(float (&v)[CC], const float* __restrict__ sc, uint32_t idx, int C, int ch0) {
-    const float* row = sc + (size_t)idx * (size_t)C + ch0;
-    if constexpr (VEC) {
-#pragma unroll
-        for (int q = 0; q < CC / 4; ++q) {
-            const float4 f = __ldg(reinterpret_cast<const float4*>(row) + q);
-            v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-        }
-    } else {
-#pragma unroll
-        for (int ch = 0; ch < CC; ++ch) v[ch] = __ldg(row + ch);
-    }
-}
-
-template <int CC, bool VEC, bool TABLE, int OP>
-__device__ __forceinline__ void cross_slot(const DevGrid& g, const uint32_t* table_row, const Slot& d, uint32_t index,
-                                           const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
-    uint32_t st[kCrossTaps];
-    resolve_cross<TABLE>(g, table_row, d, st);
-    float acc[CC], v[CC];
-#pragma unroll
-    for (int ch = 0; ch < CC; ++ch) acc[ch] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kCrossTaps; ++j) {
-        if (OP == VBM_CROSS_LAPLACIAN && j == 3) continue;  // the centre enters below
-        if (st[j]) {
-            load_row<CC, VEC>(v, sc, st[j], C, ch0);
-#pragma unroll
-            for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], v[ch]);
-        }
-    }
-    if constexpr (OP == VBM_CROSS_LAPLACIAN) {
-        load_row<CC, VEC>(v, sc, index, C, ch0);
-#pragma unroll
-        for (int ch = 0; ch < CC; ++ch) acc[ch] = __fsub_rn(acc[ch], __fmul_rn(6.0f, v[ch]));
-    }
-    float* row = out + (size_t)index * (size_t)C + ch0;
-    if constexpr (VEC) {
-#pragma unroll
-        for (int q = 0; q < CC / 4; ++q)
-            reinterpret_cast<float4*>(row)[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-    } else {
-#pragma unroll
-        for (int ch = 0; ch < CC; ++ch) row[ch] = acc[ch];
-    }
-}
 
 template <int CC, bool VEC, bool CACHED, int OP>
 __global__ void __launch_bounds__(512) cross_filter_kernel(DevGrid g, const float* __restrict__ sc,

@@ -16,7 +16,7 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-RESOLVERS = [vbm.RESOLVE_TREEWALK, vbm.RESOLVE_CACHED]
+RESOLVERS = [vbm.RESOLVE_TREEWALK, vbm.RESOLVE_CACHED, vbm.RESOLVE_BRICK]
 OUTPUTS = [vbm.OUTPUT_STREAMED, vbm.OUTPUT_MATERIALISED]
 
 
@@ -57,6 +57,7 @@ def test_shell_taps(shell, log2w):
         walk = gu.taps(g, shape, vbm.RESOLVE_TREEWALK)
         cached = gu.taps(g, shape, vbm.RESOLVE_CACHED)
         np.testing.assert_array_equal(walk, cached)
+        np.testing.assert_array_equal(gu.taps(g, shape, vbm.RESOLVE_BRICK), cached)
         np.testing.assert_array_equal(cached[which], o.taps(shape, which=which))
         assert (cached[0] == 0).all()
 
@@ -70,7 +71,7 @@ def test_shell_box_filter(shell, C, log2w):
     sd = gu.to_dev(s)
     ref = gu.bits(gu.box_filter(g, sd, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
     for r in RESOLVERS:
-        for out in OUTPUTS:
+        for out in (OUTPUTS if r != vbm.RESOLVE_BRICK else OUTPUTS[:1]):
             if (r, out) == (vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED):
                 continue
             np.testing.assert_array_equal(gu.bits(gu.box_filter(g, sd, C, r, out)), ref)
@@ -122,6 +123,8 @@ def test_fog_box_filter():
     cached = gu.bits(gu.box_filter(g, sd, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
     walk = gu.bits(gu.box_filter(g, sd, C, vbm.RESOLVE_TREEWALK, vbm.OUTPUT_STREAMED))
     np.testing.assert_array_equal(cached, walk)
+    brick = gu.bits(gu.box_filter(g, sd, C, vbm.RESOLVE_BRICK, vbm.OUTPUT_STREAMED))
+    np.testing.assert_array_equal(brick, walk)
     which = _sample(o.n, k=6000)
     want = gu.bits(o.box_filter(s, C, which=which)).reshape(-1, C)
     np.testing.assert_array_equal(cached.reshape(-1, C)[which], want)
