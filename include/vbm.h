@@ -87,6 +87,8 @@ extern "C" {
 #define VBM_EXPORT_LEAF_ORIGIN 3  /* n_leaves x 3 int32: leaf origin (multiple of 8) */
 #define VBM_EXPORT_BLOCK_FIRST_LEAF 4 /* n_blocks uint32: firstLeafID */
 #define VBM_EXPORT_BLOCK_JUMP 5   /* n_blocks x (W/64) uint64: jumpMap, bit s in word s/64 */
+#define VBM_EXPORT_LEAF_NEIGHBOURS 6 /* n_leaves x 32 uint32: entry (dx+1)*9+(dy+1)*3+(dz+1) = id of the leaf
+                                        at origin + 8*(dx,dy,dz) or 0xFFFFFFFF; entries 27..31 unused */
 
 typedef struct vbm_grid vbm_grid;
 

@@ -35,6 +35,7 @@ EXPORT = {
     "leaf_origin": (_K["VBM_EXPORT_LEAF_ORIGIN"], np.int32, 3),
     "block_first_leaf": (_K["VBM_EXPORT_BLOCK_FIRST_LEAF"], np.uint32, 1),
     "block_jump": (_K["VBM_EXPORT_BLOCK_JUMP"], np.uint64, None),
+    "leaf_neighbours": (_K["VBM_EXPORT_LEAF_NEIGHBOURS"], np.uint32, 32),
 }
 BOX_TAPS = 27
 CROSS_TAPS = 7

@@ -51,13 +51,14 @@ int upload(vbm_grid* g, cudaStream_t stream) {
         size_t bytes;
         size_t off;
     };
-    Part parts[6] = {
+    Part parts[7] = {
         {g->leaves.data(), g->leaves.size() * sizeof(vbm::LeafRec), 0},
         {g->root_keys.data(), g->root_keys.size() * sizeof(uint64_t), 0},
         {g->upper.data(), g->upper.size() * sizeof(uint32_t), 0},
         {g->lower.data(), g->lower.size() * sizeof(uint32_t), 0},
         {g->first_leaf.data(), g->first_leaf.size() * sizeof(uint32_t), 0},
         {g->jump.data(), g->jump.size() * sizeof(uint64_t), 0},
+        {g->nbr.data(), g->nbr.size() * sizeof(uint32_t), 0},
     };
     size_t total = 0;
     for (Part& p : parts) {
@@ -90,6 +91,7 @@ int upload(vbm_grid* g, cudaStream_t stream) {
     d.lower = reinterpret_cast<const uint32_t*>(base + parts[3].off);
     d.first_leaf = reinterpret_cast<const uint32_t*>(base + parts[4].off);
     d.jump = reinterpret_cast<const uint64_t*>(base + parts[5].off);
+    d.nbr = reinterpret_cast<const uint32_t*>(base + parts[6].off);
     d.n = (uint32_t)g->n;
     d.n_leaves = (uint32_t)g->n_leaves;
     d.n_blocks = (uint32_t)g->n_blocks;
@@ -195,6 +197,7 @@ int vbm_leaf_export(const vbm_grid* g, int what, void* dst, uint64_t bytes) {
         case VBM_EXPORT_LEAF_ORIGIN: need = nl * 3 * sizeof(int32_t); break;
         case VBM_EXPORT_BLOCK_FIRST_LEAF: need = g->first_leaf.size() * sizeof(uint32_t); break;
         case VBM_EXPORT_BLOCK_JUMP: need = g->jump.size() * sizeof(uint64_t); break;
+        case VBM_EXPORT_LEAF_NEIGHBOURS: need = g->nbr.size() * sizeof(uint32_t); break;
         default: return fail(VBM_ERR_INVALID, "vbm_leaf_export: unknown array");
     }
     if (bytes != need)
@@ -213,6 +216,7 @@ int vbm_leaf_export(const vbm_grid* g, int what, void* dst, uint64_t bytes) {
     }
     if (what == VBM_EXPORT_BLOCK_FIRST_LEAF && need) std::memcpy(out, g->first_leaf.data(), need);
     if (what == VBM_EXPORT_BLOCK_JUMP && need) std::memcpy(out, g->jump.data(), need);
+    if (what == VBM_EXPORT_LEAF_NEIGHBOURS && need) std::memcpy(out, g->nbr.data(), need);
     return VBM_OK;
 }
 

@@ -1,58 +1,69 @@
-// Brick resolver: per-leaf padded neighbourhoods staged in shared memory.
+// Brick resolver: per-leaf padded index bricks in shared memory, then a
+// channel-parallel gather.
 //
 // Sources (web pages; cited by title and section):
 //   [2263] OpenVDB PR #2263 "Alternative stencil resolvers for VoxelBlockManager"
 //   [2262] OpenVDB PR #2262 "NanoVDB VBM: Streaming box-stencil"
+//   [2258] OpenVDB PR #2258 "VBM select-based inverse-map decode"
 //
-// The pages' cached resolver stages, per block, a table of neighbour-leaf
-// pointers and then resolves every tap of every voxel with an in-leaf rank
-// ([2263] "Summary").  On GB300 that costs ~50 instructions per tap and 27
-// sidecar-row gathers per voxel through L1.  The brick resolver keeps the
-// pages' structure (one CTA per VBM block, slots decoded in registers by the
-// select-based decode, the same staged neighbour-leaf table, the same
-// MaxCachedLeaves fallback to the tree walk) and adds one stage: for each leaf
-// the block spans, the block builds a 10x10x10 brick covering the leaf and a
-// one-voxel halo.  Cell (bx,by,bz) holds the leaf-relative position
-// (bx-1, by-1, bz-1); its index is ranked once per z-row (one popcount for the
-// row base, one per cell), and the brick holds the sidecar values of those
-// indices (+0.0 for inactive cells).  Each voxel then reads its 27 taps at
-// fixed offsets from its own cell and adds them in tap order
-// t = (di+1)*9 + (dj+1)*3 + (dk+1) ([2262] "What changed").
+// The pages' cached resolver stages, per VBM block, a table of neighbour-leaf
+// pointers by probing the tree, then resolves every tap of every voxel with an
+// in-leaf rank ([2263] "Summary").  Measured on GB300 that costs ~1,500
+// instructions per voxel at one channel and, at 16 channels, 27 row gathers
+// per voxel that saturate L1.  This resolver keeps the pages' structure (one CTA
+// per VBM block; every slot decoded in registers by the select-based decode;
+// a block's voxels span consecutive leaves firstLeafID .. firstLeafID +
+// popcount(jumpMap)) and changes three things:
 //
-// Bit-exactness: every tap's accumulator starts at +0.0 and adds in tap
-// order.  An accumulator that starts at +0.0 is never -0.0 under
-// round-to-nearest, and x + (+0.0) == x for every such x, so adding +0.0 for
-// an inactive tap gives the same bits as skipping it.
+//  1. Neighbour-leaf ids come from the builder's per-leaf neighbour rows (27
+//     ids in one 128-byte line) instead of 27 tree probes per spanned leaf.
+//  2. For each spanned leaf the block builds a 10x10x10 brick of indices
+//     covering the leaf and a one-voxel halo.  Cell (bx,by,bz) holds the index
+//     of leaf-relative position (bx-1, by-1, bz-1), 0 if inactive.  A brick row
+//     (fixed bx,by: ten z cells) costs one mask-word load, one popcount for the
+//     row's base index and one popcount per cell (the in-leaf rank through the
+//     per-word bases, i.e. the 9-bit directory pre-added to the leaf's first
+//     index), plus one rank for each of the two halo cells.  Only the x planes
+//     that the block's voxels of that leaf touch are built, and the rows of up
+//     to kMaxGroup leaves are built together, one row per thread.
+//  3. The gather is channel-parallel: thread (voxel, channel group) reads the
+//     voxel's 27 tap indices from the brick at fixed offsets from its own cell,
+//     in tap order t = (di+1)*9 + (dj+1)*3 + (dk+1), and adds
+//     sidecar[idx*C + ch] for each non-zero tap ([2262] "What changed"), so the
+//     lanes of one voxel read one contiguous sidecar row together.
 //
-// Only the brick planes that the block's voxels of that leaf touch are built
-// (the leaf's voxels in the block cover a contiguous run of in-leaf offsets,
-// hence a range of x planes).  Channels are processed in chunks of CCH: with
-// one chunk the values are gathered while the row indices are in registers;
-// with several, an index brick is built once and a value brick per chunk.
+// The adds per voxel and channel are the same as the other resolvers', in the
+// same order, so the results are identical bit for bit.  There is no
+// MaxCachedLeaves limit: blocks spanning more than kMaxGroup leaves are built
+// in several rounds.
 #include "vbm_launch.h"
 #include "vbm_stencil.cuh"
 
 namespace vbm {
 namespace {
 
-constexpr int kEdge = 10;        // brick edge: leaf-relative -1..8
+constexpr int kEdge = 10;  // brick edge: leaf-relative -1..8
 constexpr int kCells = kEdge * kEdge * kEdge;
 
-// The 10 indices of brick row (bx, by) of the leaf whose neighbour-table row is
-// `trow` (27 leaf ids, (dx+1)*9 + (dy+1)*3 + (dz+1)).  Cell k holds
+// Leaves whose bricks are built in one round, by block width (shared memory
+// kMaxGroup * 4000 bytes).
+__host__ __device__ constexpr int max_group(int log2w) { return log2w <= 7 ? 4 : log2w == 8 ? 6 : 8; }
+
+// The 10 indices of brick row (bx, by) of the leaf whose neighbour row is
+// `nrow` (27 leaf ids at (dx+1)*9 + (dy+1)*3 + (dz+1)).  Cell k holds
 // leaf-relative z = k-1: cells 1..8 from the leaf at (dx,dy,0), cell 0 from
 // (dx,dy,-1) (its z = 7) and cell 9 from (dx,dy,+1) (its z = 0).
-__device__ __forceinline__ void brick_row(const LeafRec* __restrict__ leaves, const uint32_t* trow, int bx, int by,
-                                          uint32_t (&idx)[kEdge]) {
-    const int rx = bx - 1, ry = by - 1;                 // -1..8
-    const int sx = (rx >> 3) + 1, sy = (ry >> 3) + 1;   // 0..2
-    const uint32_t xw = (uint32_t)(rx & 7);             // mask word of plane x
-    const uint32_t yb = (uint32_t)(ry & 7) * 8u;        // first bit of the z-row
-    const uint32_t* col = trow + sx * 9 + sy * 3;
+__device__ __forceinline__ void brick_row(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ nrow, int bx,
+                                          int by, uint32_t (&idx)[kEdge]) {
+    const int rx = bx - 1, ry = by - 1;                // -1..8
+    const int sx = (rx >> 3) + 1, sy = (ry >> 3) + 1;  // 0..2
+    const uint32_t xw = (uint32_t)(rx & 7);            // mask word of plane x
+    const uint32_t yb = (uint32_t)(ry & 7) * 8u;       // first bit of the z-row
+    const uint32_t* col = nrow + sx * 9 + sy * 3;
+    const uint32_t Lm = __ldg(col), L0 = __ldg(col + 1), Lp = __ldg(col + 2);
     uint32_t byte = 0, rb = 0;
-    const uint32_t L = col[1];
-    if (L != kNone) {
-        const LeafRec* r = leaves + L;
+    if (L0 != kNone) {
+        const LeafRec* r = leaves + L0;
         const uint64_t word = __ldg(&r->mask[xw]);
         byte = (uint32_t)(word >> yb) & 0xFFu;
         rb = __ldg(&r->base[xw]) + (uint32_t)__popcll(word & ((1ull << yb) - 1ull));
@@ -60,92 +71,35 @@ __device__ __forceinline__ void brick_row(const LeafRec* __restrict__ leaves, co
 #pragma unroll
     for (int z = 0; z < 8; ++z)
         idx[1 + z] = ((byte >> z) & 1u) ? rb + (uint32_t)__popc(byte & ((1u << z) - 1u)) : 0u;
-    const uint32_t Lm = col[0], Lp = col[2];
     idx[0] = Lm != kNone ? leaf_index_at(leaves, Lm, xw * 64u + yb + 7u) : 0u;
     idx[kEdge - 1] = Lp != kNone ? leaf_index_at(leaves, Lp, xw * 64u + yb) : 0u;
 }
 
-// Sidecar chunk of one index into shared memory (zeros for index 0).
-template <int CCH, bool VEC>
-__device__ __forceinline__ void put_value(float* __restrict__ vb, int cell, const float* __restrict__ sc, uint32_t idx,
-                                          int C, int ch0) {
-    float v[CCH];
-    if (idx) {
-        load_row<CCH, VEC>(v, sc, idx, C, ch0);
-    } else {
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) v[k] = 0.0f;
-    }
-    if constexpr (CCH == 4) {
-        reinterpret_cast<float4*>(vb)[cell] = make_float4(v[0], v[1], v[2], v[3]);
-    } else if constexpr (CCH == 2) {
-        reinterpret_cast<float2*>(vb)[cell] = make_float2(v[0], v[1]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) vb[cell * CCH + k] = v[k];
-    }
+// Brick cell of a voxel's own position (its (0,0,0) tap).
+__device__ __forceinline__ int own_cell(uint32_t off) {
+    return (int)(((off >> 6) + 1u) * 100u + (((off >> 3) & 7u) + 1u) * 10u + (off & 7u) + 1u);
 }
 
-template <int CCH>
-__device__ __forceinline__ void get_value(float (&v)[CCH], const float* __restrict__ vb, int cell) {
-    if constexpr (CCH == 4) {
-        const float4 f = reinterpret_cast<const float4*>(vb)[cell];
-        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else if constexpr (CCH == 2) {
-        const float2 f = reinterpret_cast<const float2*>(vb)[cell];
-        v[0] = f.x; v[1] = f.y;
-    } else {
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) v[k] = vb[cell * CCH + k];
-    }
-}
+__device__ __forceinline__ constexpr int box_cell_delta(int t) { return (t / 9 - 1) * 100 + ((t / 3) % 3 - 1) * 10 + (t % 3 - 1); }
+__device__ __forceinline__ constexpr int cross_cell_delta(int j) { return cross_di(j) * 100 + cross_dj(j) * 10 + cross_dk(j); }
 
-// Consumers reading a value brick; `cc` is the voxel's own cell.
-template <int CCH>
-__device__ __forceinline__ void brick_box(const float* __restrict__ vb, int cc, float (&acc)[CCH]) {
-    float v[CCH];
-#pragma unroll
-    for (int k = 0; k < CCH; ++k) acc[k] = 0.0f;
-#pragma unroll
-    for (int t = 0; t < kBoxTaps; ++t) {
-        get_value<CCH>(v, vb, cc + (t / 9 - 1) * 100 + ((t / 3) % 3 - 1) * 10 + (t % 3 - 1));
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) acc[k] = __fadd_rn(acc[k], v[k]);
-    }
-}
-
-template <int CCH, int OP>
-__device__ __forceinline__ void brick_cross(const float* __restrict__ vb, int cc, float (&acc)[CCH]) {
-    float v[CCH];
-#pragma unroll
-    for (int k = 0; k < CCH; ++k) acc[k] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kCrossTaps; ++j) {
-        if (OP == VBM_CROSS_LAPLACIAN && j == 3) continue;
-        get_value<CCH>(v, vb, cc + cross_di(j) * 100 + cross_dj(j) * 10 + cross_dk(j));
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) acc[k] = __fadd_rn(acc[k], v[k]);
-    }
-    if constexpr (OP == VBM_CROSS_LAPLACIAN) {
-        get_value<CCH>(v, vb, cc);
-#pragma unroll
-        for (int k = 0; k < CCH; ++k) acc[k] = __fsub_rn(acc[k], __fmul_rn(6.0f, v[k]));
-    }
-}
-
-// Shared state of a block: staged table, per-slot offsets, leaf start slots.
-struct BrickBlock {
-    uint32_t b, W, fl, span, n_valid, index;
+// Per-block state.  Shared memory (dynamic): ib[group][1000] index bricks,
+// then offs[W] (voxel offset of each slot), lof[W] (slot's leaf - firstLeafID)
+// and starts[span+1] (first slot of each spanned leaf; starts[span] = valid
+// slots).
+struct BrickCtx {
+    uint32_t b, W, fl, span, n_valid;
     const uint64_t* jb;
-    bool active;
-    Slot d;
 };
 
-// Decode the thread's slot; if the block fits the table, record its offset
-// and leaf start, stage the neighbour-leaf table and synchronise.  Returns
-// false (block-uniformly, before any barrier) when the block spans more than
-// MaxCachedLeaves leaves.
-__device__ __forceinline__ bool brick_prologue(const DevGrid& g, BrickBlock& k, uint32_t* table, uint16_t* offs,
+__host__ __device__ constexpr size_t brick_smem_bytes(int log2w) {
+    return (size_t)max_group(log2w) * kCells * sizeof(uint32_t) + (size_t)3 * ((1u << log2w) + 1) * sizeof(uint16_t);
+}
+
+// Decode every valid slot of the block (select-based decode, [2258] "What
+// changed") into offs/lof and record where each spanned leaf starts.  Ends with
+// a barrier.
+__device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
                                                uint16_t* starts) {
     k.W = 1u << g.log2w;
     const uint32_t words = k.W >> 6;
@@ -154,194 +108,198 @@ __device__ __forceinline__ bool brick_prologue(const DevGrid& g, BrickBlock& k, 
     k.fl = __ldg(&g.first_leaf[k.b]);
     k.span = block_span(k.jb, words);
     k.n_valid = min(k.W, g.n - k.b * k.W);
-    const uint32_t s = threadIdx.x;
-    k.active = s < k.n_valid;
-    k.index = 1u + k.b * k.W + s;
-    k.d.leaf = 0;
-    k.d.off = 0;
-    if (k.active) k.d = decode_slot(g, k.fl, k.jb, s, k.index);
-    if (k.span > VBM_MAX_CACHED_LEAVES) return false;
-    if (k.active) {
-        offs[s] = (uint16_t)k.d.off;
-        if (s == 0 || ((__ldg(&k.jb[s >> 6]) >> (s & 63u)) & 1ull)) starts[k.d.leaf - k.fl] = (uint16_t)s;
+    for (uint32_t s = threadIdx.x; s < k.n_valid; s += blockDim.x) {
+        const Slot d = decode_slot(g, k.fl, k.jb, s, 1u + k.b * k.W + s);
+        offs[s] = (uint16_t)d.off;
+        lof[s] = (uint16_t)(d.leaf - k.fl);
+        if (s == 0 || ((__ldg(&k.jb[s >> 6]) >> (s & 63u)) & 1ull)) starts[d.leaf - k.fl] = (uint16_t)s;
     }
-    stage_leaf_table(g, k.fl, k.span, table);
-    return true;
+    if (threadIdx.x == 0) starts[k.span] = (uint16_t)k.n_valid;
+    __syncthreads();
 }
 
-// Brick planes [x0, x1) that leaf l's voxels of this block need.
-__device__ __forceinline__ void leaf_planes(const BrickBlock& k, const uint16_t* offs, const uint16_t* starts, uint32_t l,
-                                            int& x0, int& x1) {
-    const uint32_t sb = starts[l];
-    const uint32_t se = (l + 1 < k.span) ? starts[l + 1] : k.n_valid;
-    x0 = offs[sb] >> 6;
-    x1 = (offs[se - 1] >> 6) + 3;
-}
-
-__device__ __forceinline__ int own_cell(const Slot& d) {
-    return (int)(((d.off >> 6) + 1u) * 100u + (((d.off >> 3) & 7u) + 1u) * 10u + (d.off & 7u) + 1u);
-}
-
-// Fill the value brick planes [x0,x1) for channels [ch0, ch0+CCH).  From the
-// index brick `ib` when given, else straight from the table row by rows.
-template <int CCH, bool VEC>
-__device__ __forceinline__ void fill_values(const DevGrid& g, const uint32_t* trow, const uint32_t* ib, float* vb,
-                                            int x0, int x1, const float* __restrict__ sc, int C, int ch0) {
-    if (ib) {
-        for (int c = x0 * 100 + (int)threadIdx.x; c < x1 * 100; c += (int)blockDim.x)
-            put_value<CCH, VEC>(vb, c, sc, ib[c], C, ch0);
-    } else {
-        for (int r = x0 * 10 + (int)threadIdx.x; r < x1 * 10; r += (int)blockDim.x) {
-            uint32_t idx[kEdge];
-            brick_row(g.leaves, trow, r / 10, r % 10, idx);
-#pragma unroll
-            for (int z = 0; z < kEdge; ++z) put_value<CCH, VEC>(vb, r * 10 + z, sc, idx[z], C, ch0);
-        }
-    }
-}
-
-__device__ __forceinline__ void fill_indices(const DevGrid& g, const uint32_t* trow, uint32_t* ib, int x0, int x1) {
-    for (int r = x0 * 10 + (int)threadIdx.x; r < x1 * 10; r += (int)blockDim.x) {
+// Build the bricks of spanned leaves l0 .. l0+nb-1 into ib[0..nb).  Leaf l's
+// voxels in this block run from slot starts[l] to starts[l+1]-1, in increasing
+// in-leaf offset (x-major), so they touch x planes x(first)-1 .. x(last)+1,
+// i.e. brick planes [x(first), x(last)+3).  One row per thread.  VALUES (one
+// channel only): store sidecar[idx] (+0.0 where idx == 0) instead of idx.
+// Ends with a barrier.
+template <bool VALUES>
+__device__ __forceinline__ void build_round(const DevGrid& g, const BrickCtx& k, const uint16_t* offs,
+                                            const uint16_t* starts, uint32_t l0, uint32_t nb, uint32_t* ib,
+                                            const float* __restrict__ sc) {
+    for (uint32_t r = threadIdx.x; r < nb * 100u; r += blockDim.x) {
+        const uint32_t kk = r / 100u, row = r - kk * 100u, l = l0 + kk;
+        const uint32_t x0 = offs[starts[l]] >> 6, x1 = (offs[starts[l + 1] - 1u] >> 6) + 3u;
+        if (row < x0 * 10u || row >= x1 * 10u) continue;
         uint32_t idx[kEdge];
-        brick_row(g.leaves, trow, r / 10, r % 10, idx);
+        brick_row(g.leaves, g.nbr + (size_t)(k.fl + l) * kNbrStride, (int)(row / 10u), (int)(row % 10u), idx);
+        uint32_t* dst = ib + kk * kCells + row * kEdge;
+        if constexpr (VALUES) {
+            float v[kEdge];
 #pragma unroll
-        for (int z = 0; z < kEdge; ++z) ib[r * 10 + z] = idx[z];
+            for (int z = 0; z < kEdge; ++z) v[z] = idx[z] ? __ldg(sc + idx[z]) : 0.0f;
+#pragma unroll
+            for (int z = 0; z < kEdge; ++z) dst[z] = __float_as_uint(v[z]);
+        } else {
+#pragma unroll
+            for (int z = 0; z < kEdge; ++z) dst[z] = idx[z];
+        }
     }
+    __syncthreads();
 }
 
-// KIND 0: 27-tap box; 1: cross Laplacian; 2: cross 7-tap sum.
-template <int KIND, int CCH>
-__device__ __forceinline__ void brick_consume(const float* vb, int cc, float (&acc)[CCH]) {
-    if constexpr (KIND == 0) brick_box<CCH>(vb, cc, acc);
-    else if constexpr (KIND == 1) brick_cross<CCH, VBM_CROSS_LAPLACIAN>(vb, cc, acc);
-    else brick_cross<CCH, VBM_CROSS_SUM>(vb, cc, acc);
-}
-
-// Filter kernel.  Channels [ch_begin, ch_end) in chunks of CCH; MULTI: more
-// than one chunk (index brick + value brick per chunk).
-template <int KIND, int CCH, bool VEC, bool MULTI>
-__global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
-                                                           float* __restrict__ out, int C, int ch_begin, int ch_end) {
-    __shared__ uint32_t table[VBM_MAX_CACHED_LEAVES * kBoxTaps];
-    __shared__ uint16_t offs[512];
-    __shared__ uint16_t starts[VBM_MAX_CACHED_LEAVES];
-    __shared__ uint32_t ib[MULTI ? kCells : 1];
-    __shared__ __align__(16) float vb[kCells * CCH];
-
-    BrickBlock k;
-    if (!brick_prologue(g, k, table, offs, starts)) {
-        // MaxCachedLeaves fallback: per-tap tree walk, gathers from global memory.
-        if (k.active) {
-            for (int ch0 = ch_begin; ch0 < ch_end; ch0 += CCH) {
-                if constexpr (KIND == 0) box_slot<CCH, VEC, false, false>(g, nullptr, k.d, k.index, sc, out, C, ch0);
-                else if constexpr (KIND == 1)
-                    cross_slot<CCH, VEC, false, VBM_CROSS_LAPLACIAN>(g, nullptr, k.d, k.index, sc, out, C, ch0);
-                else cross_slot<CCH, VEC, false, VBM_CROSS_SUM>(g, nullptr, k.d, k.index, sc, out, C, ch0);
-            }
+// KIND 0: 27-tap box; 1: cross Laplacian; 2: cross 7-tap sum.  Channels
+// [ch0, ch0+CC) of one voxel whose own brick cell is `cc` in brick `ibk`.
+template <int KIND, int CC, bool VEC>
+__device__ __forceinline__ void brick_consume(const uint32_t* __restrict__ ibk, int cc, uint32_t index,
+                                              const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
+    float acc[CC];
+#pragma unroll
+    for (int c = 0; c < CC; ++c) acc[c] = 0.0f;
+    if constexpr (KIND == 0) {
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t) {
+            const uint32_t idx = ibk[cc + box_cell_delta(t)];
+            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
         }
     } else {
-        const uint32_t my_l = k.d.leaf - k.fl;
-        const int cc = own_cell(k.d);
-        for (uint32_t l = 0; l < k.span; ++l) {
-            int x0, x1;
-            leaf_planes(k, offs, starts, l, x0, x1);
-            const uint32_t* trow = table + l * kBoxTaps;
-            const bool mine = k.active && my_l == l;
-            if constexpr (MULTI) {
-                fill_indices(g, trow, ib, x0, x1);
-                __syncthreads();
-            }
-            for (int ch0 = ch_begin; ch0 < ch_end; ch0 += CCH) {
-                fill_values<CCH, VEC>(g, trow, MULTI ? ib : nullptr, vb, x0, x1, sc, C, ch0);
-                __syncthreads();
-                if (mine) {
-                    float acc[CCH];
-                    brick_consume<KIND, CCH>(vb, cc, acc);
-                    store_row<CCH, VEC>(out, k.index, C, ch0, acc);
-                }
-                __syncthreads();
-            }
+#pragma unroll
+        for (int j = 0; j < kCrossTaps; ++j) {
+            if (KIND == 1 && j == 3) continue;  // the Laplacian's centre enters below
+            const uint32_t idx = ibk[cc + cross_cell_delta(j)];
+            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
+        }
+        if constexpr (KIND == 1) {
+            float v[CC];
+            load_row<CC, VEC>(v, sc, index, C, ch0);
+#pragma unroll
+            for (int c = 0; c < CC; ++c) acc[c] = __fsub_rn(acc[c], __fmul_rn(6.0f, v[c]));
         }
     }
-    if (blockIdx.x == 0 && (int)threadIdx.x < ch_end - ch_begin) out[ch_begin + threadIdx.x] = 0.0f;
+    store_row<CC, VEC>(out, index, C, ch0, acc);
 }
 
-// Raw taps through the index brick.  SHAPE 27 (box) or 7 (cross).
+// One-channel consumers reading a value brick (+0.0 in inactive cells; adding
+// +0.0 to an fp32 sum that started at +0.0 leaves it unchanged bit for bit).
+template <int KIND>
+__device__ __forceinline__ float brick_consume_values(const uint32_t* __restrict__ vbk, int cc) {
+    float acc = 0.0f;
+    if constexpr (KIND == 0) {
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t) acc = __fadd_rn(acc, __uint_as_float(vbk[cc + box_cell_delta(t)]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kCrossTaps; ++j) {
+            if (KIND == 1 && j == 3) continue;
+            acc = __fadd_rn(acc, __uint_as_float(vbk[cc + cross_cell_delta(j)]));
+        }
+        if constexpr (KIND == 1) acc = __fsub_rn(acc, __fmul_rn(6.0f, __uint_as_float(vbk[cc])));
+    }
+    return acc;
+}
+
+struct BrickSmem {
+    uint32_t* ib;
+    uint16_t *offs, *lof, *starts;
+    uint32_t group;
+};
+
+__device__ __forceinline__ BrickSmem carve(unsigned char* smem, int log2w) {
+    BrickSmem m;
+    const uint32_t W1 = (1u << log2w) + 1u;
+    m.group = (uint32_t)max_group(log2w);
+    m.ib = reinterpret_cast<uint32_t*>(smem);
+    m.offs = reinterpret_cast<uint16_t*>(m.ib + m.group * kCells);
+    m.lof = m.offs + W1;
+    m.starts = m.lof + W1;
+    return m;
+}
+
+// Filter kernel: channels [ch_begin, ch_begin + lanes*CC); `lanes` threads per
+// voxel, each handling CC consecutive channels (VEC: as float4s).  VALUES: one
+// channel, value bricks (lanes == CC == 1).
+template <int KIND, int CC, bool VEC, bool VALUES>
+__global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
+                                                           float* __restrict__ out, int C, int ch_begin, int lanes) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const BrickSmem m = carve(smem, g.log2w);
+    BrickCtx k;
+    brick_prologue(g, k, m.offs, m.lof, m.starts);
+    const uint32_t L = (uint32_t)lanes;
+    for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
+        const uint32_t nb = min(m.group, k.span - l0);
+        build_round<VALUES>(g, k, m.offs, m.starts, l0, nb, m.ib, sc);
+        const uint32_t sb = m.starts[l0], se = m.starts[l0 + nb];
+        if constexpr (VALUES) {
+            for (uint32_t s = sb + threadIdx.x; s < se; s += blockDim.x) {
+                const uint32_t* vbk = m.ib + (uint32_t)(m.lof[s] - l0) * kCells;
+                out[1u + k.b * k.W + s] = brick_consume_values<KIND>(vbk, own_cell(m.offs[s]));
+            }
+        } else {
+            const uint32_t items = (se - sb) * L;
+            for (uint32_t it = threadIdx.x; it < items; it += blockDim.x) {
+                const uint32_t v = L == 1 ? it : it / L, q = it - v * L, s = sb + v;
+                const uint32_t* ibk = m.ib + (uint32_t)(m.lof[s] - l0) * kCells;
+                brick_consume<KIND, CC, VEC>(ibk, own_cell(m.offs[s]), 1u + k.b * k.W + s, sc, out, C,
+                                             ch_begin + (int)(q * CC));
+            }
+        }
+        __syncthreads();  // the next round overwrites the bricks
+    }
+    if (blockIdx.x == 0 && threadIdx.x < L * CC) out[ch_begin + threadIdx.x] = 0.0f;
+}
+
+// Raw taps through the index bricks.  SHAPE 27 (box) or 7 (cross).
 template <int SHAPE>
 __global__ void __launch_bounds__(512) brick_taps_kernel(DevGrid g, uint32_t* __restrict__ taps) {
-    __shared__ uint32_t table[VBM_MAX_CACHED_LEAVES * kBoxTaps];
-    __shared__ uint16_t offs[512];
-    __shared__ uint16_t starts[VBM_MAX_CACHED_LEAVES];
-    __shared__ uint32_t ib[kCells];
-
-    BrickBlock k;
-    if (!brick_prologue(g, k, table, offs, starts)) {
-        if (k.active) {
-            uint32_t* row = taps + (size_t)k.index * SHAPE;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const BrickSmem m = carve(smem, g.log2w);
+    BrickCtx k;
+    brick_prologue(g, k, m.offs, m.lof, m.starts);
+    for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
+        const uint32_t nb = min(m.group, k.span - l0);
+        build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
+        for (uint32_t s = m.starts[l0] + threadIdx.x; s < m.starts[l0 + nb]; s += blockDim.x) {
+            const uint32_t* ibk = m.ib + (uint32_t)(m.lof[s] - l0) * kCells;
+            const int cc = own_cell(m.offs[s]);
+            uint32_t* row = taps + (size_t)(1u + k.b * k.W + s) * SHAPE;
             if constexpr (SHAPE == kBoxTaps) {
-                const TapResolver<false> resolve(g, nullptr, k.d);
 #pragma unroll
-                for (int t = 0; t < kBoxTaps; ++t) row[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
+                for (int t = 0; t < kBoxTaps; ++t) row[t] = ibk[cc + box_cell_delta(t)];
             } else {
-                uint32_t st[kCrossTaps];
-                resolve_cross<false>(g, nullptr, k.d, st);
 #pragma unroll
-                for (int j = 0; j < kCrossTaps; ++j) row[j] = st[j];
+                for (int j = 0; j < kCrossTaps; ++j) row[j] = ibk[cc + cross_cell_delta(j)];
             }
         }
-    } else {
-        const uint32_t my_l = k.d.leaf - k.fl;
-        const int cc = own_cell(k.d);
-        for (uint32_t l = 0; l < k.span; ++l) {
-            int x0, x1;
-            leaf_planes(k, offs, starts, l, x0, x1);
-            fill_indices(g, table + l * kBoxTaps, ib, x0, x1);
-            __syncthreads();
-            if (k.active && my_l == l) {
-                uint32_t* row = taps + (size_t)k.index * SHAPE;
-                if constexpr (SHAPE == kBoxTaps) {
-#pragma unroll
-                    for (int t = 0; t < kBoxTaps; ++t)
-                        row[t] = ib[cc + (t / 9 - 1) * 100 + ((t / 3) % 3 - 1) * 10 + (t % 3 - 1)];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < kCrossTaps; ++j) row[j] = ib[cc + cross_di(j) * 100 + cross_dj(j) * 10 + cross_dk(j)];
-                }
-            }
-            __syncthreads();
-        }
+        __syncthreads();
     }
     if (blockIdx.x == 0 && threadIdx.x < (unsigned)SHAPE) taps[threadIdx.x] = 0u;
 }
 
-template <int KIND, int CCH, bool VEC, bool MULTI>
-cudaError_t launch_brick(const DevGrid& g, const float* sc, int C, int ch_begin, int ch_end, float* out,
-                         cudaStream_t stream) {
-    brick_filter_kernel<KIND, CCH, VEC, MULTI>
-        <<<g.n_blocks, threads_for(g.log2w), 0, stream>>>(g, sc, out, C, ch_begin, ch_end);
+template <int KIND, int CC, bool VEC, bool VALUES>
+cudaError_t launch_brick(const DevGrid& g, const float* sc, int C, int lanes, float* out, cudaStream_t stream) {
+    brick_filter_kernel<KIND, CC, VEC, VALUES>
+        <<<g.n_blocks, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(g, sc, out, C, 0, lanes);
     return cudaGetLastError();
 }
+
+// Channel layout per C: one channel -> value bricks; 2 or 3 -> one lane with
+// all channels; multiples of 4 -> lanes of kVecChannels channels read as
+// float4s; anything else -> one lane per channel.
+constexpr int kVecChannels = 4;
 
 template <int KIND>
 cudaError_t launch_brick_kind(const DevGrid& g, const float* sc, int C, float* out, cudaStream_t stream) {
     switch (C) {
-        case 1: return launch_brick<KIND, 1, false, false>(g, sc, C, 0, 1, out, stream);
-        case 2: return launch_brick<KIND, 2, false, false>(g, sc, C, 0, 2, out, stream);
-        case 3: return launch_brick<KIND, 3, false, false>(g, sc, C, 0, 3, out, stream);
-        case 4: return launch_brick<KIND, 4, true, false>(g, sc, C, 0, 4, out, stream);
+        case 1: return launch_brick<KIND, 1, false, true>(g, sc, C, 1, out, stream);
+        case 2: return launch_brick<KIND, 2, false, false>(g, sc, C, 1, out, stream);
+        case 3: return launch_brick<KIND, 3, false, false>(g, sc, C, 1, out, stream);
         default: break;
     }
-    if (C % 4 == 0) return launch_brick<KIND, 4, true, true>(g, sc, C, 0, C, out, stream);
-    // Rows are not 16-byte aligned: scalar loads; chunks of 4, then the rest.
-    const int q = C / 4 * 4;
-    cudaError_t e = q > 4 ? launch_brick<KIND, 4, false, true>(g, sc, C, 0, q, out, stream)
-                          : launch_brick<KIND, 4, false, false>(g, sc, C, 0, 4, out, stream);
-    if (e != cudaSuccess) return e;
-    switch (C - q) {
-        case 1: return launch_brick<KIND, 1, false, false>(g, sc, C, q, C, out, stream);
-        case 2: return launch_brick<KIND, 2, false, false>(g, sc, C, q, C, out, stream);
-        default: return launch_brick<KIND, 3, false, false>(g, sc, C, q, C, out, stream);
-    }
+    if (C % kVecChannels == 0) return launch_brick<KIND, kVecChannels, true, false>(g, sc, C, C / kVecChannels, out, stream);
+    if (C % 4 == 0) return launch_brick<KIND, 4, true, false>(g, sc, C, C / 4, out, stream);
+    return launch_brick<KIND, 1, false, false>(g, sc, C, C, out, stream);
 }
 
 }  // namespace
@@ -356,8 +314,10 @@ cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, fl
 }
 
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream) {
-    if (shape == kBoxTaps) brick_taps_kernel<kBoxTaps><<<g.n_blocks, threads_for(g.log2w), 0, stream>>>(g, taps);
-    else brick_taps_kernel<kCrossTaps><<<g.n_blocks, threads_for(g.log2w), 0, stream>>>(g, taps);
+    const size_t smem = brick_smem_bytes(g.log2w);
+    const unsigned threads = (unsigned)threads_for(g.log2w);
+    if (shape == kBoxTaps) brick_taps_kernel<kBoxTaps><<<g.n_blocks, threads, smem, stream>>>(g, taps);
+    else brick_taps_kernel<kCrossTaps><<<g.n_blocks, threads, smem, stream>>>(g, taps);
     return cudaGetLastError();
 }
 

@@ -56,6 +56,17 @@ class LeafTable {
         }
     }
 
+    // Id of the leaf at (x,y,z), or kNone.
+    uint32_t find(int32_t x, int32_t y, int32_t z) const {
+        size_t h = slot_of(x, y, z);
+        for (;;) {
+            uint32_t id = ids_[h];
+            if (id == kNone) return kNone;
+            if (keys_[3 * h] == x && keys_[3 * h + 1] == y && keys_[3 * h + 2] == z) return id;
+            h = (h + 1) & (cap_ - 1);
+        }
+    }
+
    private:
     static size_t next_pow2(size_t v) {
         size_t p = 1;
@@ -221,6 +232,25 @@ int build_host(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, vbm
         uint64_t f = g->leaves[l].first;
         uint64_t b = (f - 1) / W, s = (f - 1) % W;
         if (s != 0) g->jump[b * words + s / 64] |= (uint64_t)1 << (s % 64);
+    }
+    // 6. Neighbour rows: nbr[L*32 + (dx+1)*9 + (dy+1)*3 + (dz+1)] = id of the leaf
+    //    at origin(L) + 8*(dx,dy,dz), or kNone; entries 27..31 are padding.  The
+    //    GB300 brick resolver reads these instead of probing the tree per block.
+    {
+        LeafTable final_ids(nl + 16);
+        for (size_t l = 0; l < nl; ++l) {
+            bool ins = false;
+            final_ids.find_or_insert(g->leaves[l].origin[0], g->leaves[l].origin[1], g->leaves[l].origin[2],
+                                     (uint32_t)l, ins);
+        }
+        g->nbr.assign(nl * kNbrStride, kNone);
+        for (size_t l = 0; l < nl; ++l) {
+            const int32_t* o = g->leaves[l].origin;
+            for (int t = 0; t < 27; ++t) {
+                const int32_t x = o[0] + 8 * (t / 9 - 1), y = o[1] + 8 * ((t / 3) % 3 - 1), z = o[2] + 8 * (t % 3 - 1);
+                g->nbr[l * kNbrStride + t] = final_ids.find(x, y, z);
+            }
+        }
     }
     g->n_over_cache = 0;
     g->max_span = 0;

@@ -25,6 +25,7 @@ constexpr int kLowerSlots = 16 * 16 * 16;   // children of a lower node (leaves)
 constexpr int kBoxTaps = 27;
 constexpr int kCrossTaps = 7;
 constexpr int kMaxC = 64;
+constexpr int kNbrStride = 32;              // neighbour-row stride: 27 ids + 5 pad = one 128-byte line
 
 // One leaf: 128 bytes, one cache line.  `mask` is the 512-bit value mask (bit
 // off%64 of word off/64, off = x*64 + y*8 + z in-leaf); `prefix` is the 9-bit
@@ -59,6 +60,7 @@ struct DevGrid {
     const uint32_t* lower;       // n_lower x 4096: leaf id or kNone
     const uint32_t* first_leaf;  // n_blocks
     const uint64_t* jump;        // n_blocks x (W/64)
+    const uint32_t* nbr;         // n_leaves x kNbrStride: neighbour-leaf ids (see vbm_build.cpp)
     uint32_t n;                  // active voxels
     uint32_t n_leaves;
     uint32_t n_blocks;
@@ -83,6 +85,7 @@ struct vbm_grid {
     std::vector<uint32_t> lower;
     std::vector<uint32_t> first_leaf;
     std::vector<uint64_t> jump;
+    std::vector<uint32_t> nbr;
     // device arena (one allocation) and the views into it
     void* arena = nullptr;
     size_t arena_bytes = 0;

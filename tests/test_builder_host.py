@@ -52,6 +52,22 @@ def test_leaves_match_oracle(case):
         np.testing.assert_array_equal(field.astype(np.int64), counts[:, :w].sum(axis=1))
 
 
+def test_neighbour_rows(case):
+    """Entry (dx+1)*9+(dy+1)*3+(dz+1) of leaf L is the leaf 8*(dx,dy,dz) away."""
+    coords, o = case
+    g = _host_grid(coords, 7)
+    _, origins = o.leaves()
+    where = {tuple(p): i for i, p in enumerate(origins.tolist())}
+    nbr = vbm.vbm_leaf_export(g, "leaf_neighbours")
+    assert nbr.shape == (len(origins), 32)
+    assert (nbr[:, 27:] == 0xFFFFFFFF).all()
+    for L, (x, y, z) in enumerate(origins.tolist()):
+        for t in range(27):
+            want = where.get((x + 8 * (t // 9 - 1), y + 8 * ((t // 3) % 3 - 1), z + 8 * (t % 3 - 1)), 0xFFFFFFFF)
+            assert nbr[L, t] == want
+        assert nbr[L, 13] == L
+
+
 @pytest.mark.parametrize("log2w", [6, 7, 8, 9])
 def test_block_metadata_matches_oracle(case, log2w):
     coords, o = case
