@@ -60,9 +60,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     jobs = []
+    # Optional extra nvcc flags (e.g. -D tuning constants) from VBM_NVCC_FLAGS.
+    extra = os.environ.get("VBM_NVCC_FLAGS", "").split()
     for src in CU_SOURCES:
         obj = os.path.join(BUILD, src + ".o")
-        cmd = [nvcc, "-std=c++20", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+        cmd = [nvcc, "-std=c++20", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC", "-Xptxas", "-v", *extra,
                "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         jobs.append((cmd, obj, os.path.join(BUILD, src + ".log")))
     for src in CPP_SOURCES:

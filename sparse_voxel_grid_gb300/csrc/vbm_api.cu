@@ -97,6 +97,8 @@ int upload(vbm_grid* g, cudaStream_t stream) {
     d.n_blocks = (uint32_t)g->n_blocks;
     d.n_upper = g->n_upper;
     d.log2w = g->log2w;
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, g->device);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: cudaDeviceGetAttribute", e);
     return VBM_OK;
 }
 

@@ -1,32 +1,112 @@
 // Select-based inverse-map decode kernel (OpenVDB PR #2258 "VBM select-based
-// inverse-map decode", "What changed"): one thread per output slot; each slot
-// ranks itself into its leaf with a jumpMap popcount and finds its voxel by a
-// select into the leaf mask through the 9-bit prefix directory.  No shared
-// memory, no barrier.  Output is structure-of-arrays: a 32-bit leaf index and
-// a 16-bit voxel offset per slot, written coalesced.
+// inverse-map decode", "What changed"): every output slot ranks itself into
+// its leaf with a jumpMap popcount and finds its voxel by a select into the
+// leaf mask through the 9-bit prefix directory.  O(1) per slot.  Output is
+// structure-of-arrays: a 32-bit leaf index and a 16-bit voxel offset per slot,
+// written coalesced.
+//
+// GB300 layout.  The work per slot is tiny; what bounds the kernel is the
+// chain of dependent loads (block metadata -> leaf record -> mask word) and
+// how many such chains are in flight.  So:
+//   - one resident wave of CTAs, each owning an equal contiguous slot range
+//     (no tail wave);
+//   - the CTA stages the firstLeafID and jumpMap words of the blocks its range
+//     overlaps in shared memory, with per-word popcount prefixes, so the rank
+//     is a shared-memory lookup plus one popcount;
+//   - each thread decodes up to kMaxPerThread slots in explicit stages (all
+//     leaf-record loads, then all mask-word loads, then the selects), so its
+//     chains overlap instead of running one after another.
 #include "vbm_device.cuh"
 #include "vbm_launch.h"
 
 namespace vbm {
 namespace {
 
-__global__ void __launch_bounds__(512) decode_kernel(DevGrid g, uint32_t* __restrict__ leaf_index,
-                                                     uint16_t* __restrict__ voxel_offset) {
-    const uint32_t W = 1u << g.log2w;
-    const uint32_t b = blockIdx.x;
-    const uint64_t* jb = g.jump + (size_t)b * (W >> 6);
-    const uint32_t fl = __ldg(&g.first_leaf[b]);
-    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
-        const uint32_t index = 1u + b * W + s;
-        const size_t slot = (size_t)b * W + s;
-        if (index > g.n) {
-            leaf_index[slot] = kNone;
-            voxel_offset[slot] = kNoOffset;
-        } else {
-            const Slot d = decode_slot(g, fl, jb, s, index);
-            leaf_index[slot] = d.leaf;
-            voxel_offset[slot] = (uint16_t)d.off;
+#ifndef VBM_DECODE_PER_THREAD
+#define VBM_DECODE_PER_THREAD 2
+#endif
+#ifndef VBM_DECODE_MIN_CTAS
+#define VBM_DECODE_MIN_CTAS 16
+#endif
+constexpr int kDecodeThreads = 128;
+constexpr int kMaxPerThread = VBM_DECODE_PER_THREAD;        // slots per thread at most
+constexpr int kMaxRange = kDecodeThreads * kMaxPerThread;   // slots per chunk
+constexpr int kMaxBlocks = kMaxRange / 64 + 2;              // blocks a chunk can overlap
+constexpr int kMaxWords = 8;                                // jumpMap words per block (W = 512)
+
+__global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_kernel(DevGrid g, uint32_t n_cta, uint32_t* __restrict__ leaf_index,
+                                                                uint16_t* __restrict__ voxel_offset) {
+    __shared__ uint32_t s_fl[kMaxBlocks];
+    __shared__ uint64_t s_jw[kMaxBlocks][kMaxWords];
+    __shared__ uint16_t s_cum[kMaxBlocks][kMaxWords];  // set bits in words 0..k-1 of the block's jumpMap
+
+    const uint32_t log2w = (uint32_t)g.log2w, W = 1u << log2w, words = W >> 6;
+    const uint64_t n_slots = (uint64_t)g.n_blocks << log2w;
+    const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta), r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta);
+    // The CTA's range [r0, r1) in chunks of at most kMaxRange slots (uniform per CTA).
+    for (uint32_t s0 = r0; s0 < r1; s0 += kMaxRange) {
+        const uint32_t s1 = min(r1, s0 + (uint32_t)kMaxRange);
+        const uint32_t b0 = s0 >> log2w, nb = ((s1 - 1u) >> log2w) - b0 + 1u;
+
+        // Stage 1: block metadata of the chunk into shared memory.
+        for (uint32_t e = threadIdx.x; e < nb * (words + 1u); e += blockDim.x) {
+            const uint32_t bl = e / (words + 1u), k = e - bl * (words + 1u);
+            if (k == 0) s_fl[bl] = __ldg(&g.first_leaf[b0 + bl]);
+            else s_jw[bl][k - 1u] = __ldg(&g.jump[(size_t)(b0 + bl) * words + (k - 1u)]);
         }
+        __syncthreads();
+        if (threadIdx.x < nb) {
+            uint32_t run = 0;
+            for (uint32_t k = 0; k < words; ++k) {
+                s_cum[threadIdx.x][k] = (uint16_t)run;
+                run += (uint32_t)__popcll(s_jw[threadIdx.x][k]);
+            }
+        }
+        __syncthreads();
+
+        // Stage 2: rank -> leaf; load every slot's leaf directory and first index.
+        uint32_t leaf[kMaxPerThread], r[kMaxPerThread];
+        uint64_t dir[kMaxPerThread];
+#pragma unroll
+        for (int k = 0; k < kMaxPerThread; ++k) {
+            const uint32_t slot = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads;
+            leaf[k] = kNone;
+            if (slot < s1 && slot < g.n) {  // index = slot + 1 <= N
+                const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
+                const uint64_t keep = (2ull << (s & 63u)) - 1ull;
+                leaf[k] = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(s_jw[bl][ws] & keep);
+                const LeafRec* rec = g.leaves + leaf[k];
+                dir[k] = __ldg(&rec->prefix);
+                r[k] = slot + 1u - __ldg(&rec->first);
+            }
+        }
+        // Stage 3: word of the r-th voxel from the 9-bit directory; load the mask words.
+        uint64_t word[kMaxPerThread];
+        uint32_t wsel[kMaxPerThread];
+#pragma unroll
+        for (int k = 0; k < kMaxPerThread; ++k) {
+            if (leaf[k] == kNone) continue;
+            uint32_t w = 0;
+#pragma unroll
+            for (int f = 1; f < 8; ++f) w += (uint32_t)(((dir[k] >> (9 * (f - 1))) & 511u) <= r[k]);
+            wsel[k] = w;
+            r[k] -= w ? (uint32_t)((dir[k] >> (9 * (w - 1))) & 511u) : 0u;
+            word[k] = __ldg(&g.leaves[leaf[k]].mask[w]);
+        }
+        // Stage 4: in-word select and coalesced stores (sentinels past N).
+#pragma unroll
+        for (int k = 0; k < kMaxPerThread; ++k) {
+            const uint32_t slot = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads;
+            if (slot >= s1) continue;
+            if (leaf[k] == kNone) {
+                leaf_index[slot] = kNone;
+                voxel_offset[slot] = kNoOffset;
+            } else {
+                leaf_index[slot] = leaf[k];
+                voxel_offset[slot] = (uint16_t)(64u * wsel[k] + select64(word[k], r[k]));
+            }
+        }
+        __syncthreads();  // the next chunk overwrites the staged metadata
     }
 }
 
@@ -34,7 +114,18 @@ __global__ void __launch_bounds__(512) decode_kernel(DevGrid g, uint32_t* __rest
 
 cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream) {
     if (g.n_blocks == 0) return cudaSuccess;
-    decode_kernel<<<g.n_blocks, threads_for(g.log2w), 0, stream>>>(g, leaf_index, voxel_offset);
+    const uint64_t n_slots = (uint64_t)g.n_blocks << g.log2w;
+    // One resident wave of CTAs, each with an equal share of the slots.
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecodeThreads, 0) != cudaSuccess || n < 1) n = 1;
+        per_sm = n;
+    }
+    uint64_t n_cta = (uint64_t)(g.sm_count > 0 ? g.sm_count : 1) * (uint64_t)per_sm;
+    const uint64_t max_cta = (n_slots + 63) / 64;  // at least 64 slots per CTA
+    if (n_cta > max_cta) n_cta = max_cta;
+    decode_kernel<<<(unsigned)n_cta, kDecodeThreads, 0, stream>>>(g, (uint32_t)n_cta, leaf_index, voxel_offset);
     return cudaGetLastError();
 }
 

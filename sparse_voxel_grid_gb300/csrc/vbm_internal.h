@@ -66,6 +66,7 @@ struct DevGrid {
     uint32_t n_blocks;
     uint32_t n_upper;
     int log2w;
+    int sm_count;                // SMs of the grid's device (for one-wave launches)
 };
 
 }  // namespace vbm
