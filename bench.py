@@ -3,9 +3,11 @@
 Workload: the sphere shell of radius 185 and thickness 3 (183.5 <= |p| <= 186.5,
 1,290,538 active voxels in 11,255 leaves), fp32 sidecars U[-1,1) with C
 interleaved channels.  One step = the 27-tap box filter (select-based decode +
-cached resolver + streamed gather/accumulate, one fused kernel) over every
-active voxel at C = 1, 3, 8 and 16, BlockWidth 128: four launches.  `value`
-counts each voxel once per channel width: 4 * N voxels per step.
+brick resolver + streamed gather/accumulate, one fused kernel) over every
+active voxel at C = 1, 3, 8 and 16, BlockWidth 512: four launches.  `value`
+counts each voxel once per channel width: 4 * N voxels per step.  The other
+resolvers (the pages' tree walk and cached table), both output modes, both
+block widths, the cross Laplacian and the decode are timed in `variants`.
 
 Timing: each launch is bracketed by CUDA events on the launching stream; L2 is
 flushed (a write of twice its size) before every launch, outside the events.
@@ -30,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 CS = (1, 3, 8, 16)
-LOG2W = 7
+LOG2W = 9
 METRIC = "active voxels/s (27-tap box filter, C=1..16) and achieved HBM GB/s vs GB300 peak"
 WORKLOAD = "S185 sphere shell 183.5<=|p|<=186.5"
 LEAF_META_BYTES = 88  # mask 64 + 9-bit directory 8 + first index 4 + origin 12
@@ -240,12 +242,21 @@ def run_gpu(args):
 
 
 def load_traffic(key):
-    """DRAM bytes per launch from a committed ncu summary, if it covers `key`
-    for the current kernel version."""
+    """DRAM bytes per launch from the committed ncu summary, if it covers `key`
+    and the kernel sources are unchanged since the counters were taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
+    h = hashlib.sha1()
+    for f in d.get("source_files", []):
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != d.get("source_sha1"):
+        return None
     return d.get(key)
 
 
@@ -389,7 +400,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--resolver", choices=["cached", "brick", "walk"], default="cached")
+    ap.add_argument("--resolver", choices=["cached", "brick", "walk"], default="brick")
     ap.add_argument("--log2w", type=int, default=LOG2W, choices=[6, 7, 8, 9])
     ap.add_argument("--cpu-sample", type=int, default=150000)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
