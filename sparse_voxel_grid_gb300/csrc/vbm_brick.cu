@@ -151,33 +151,61 @@ __device__ __forceinline__ void build_round(const DevGrid& g, const BrickCtx& k,
 
 // KIND 0: 27-tap box; 1: cross Laplacian; 2: cross 7-tap sum.  Channels
 // [ch0, ch0+CC) of one voxel whose own brick cell is `cc` in brick `ibk`.
-template <int KIND, int CC, bool VEC>
+// acc[c] += sidecar[idx*C + ch0 + c] for c < CC, written without a branch: the
+// load is predicated on idx != 0 and an inactive tap adds +0.0, which leaves
+// an accumulator that started at +0.0 unchanged bit for bit.  CT > 0: the row
+// stride C is the compile-time CT.
+template <int CC, bool VEC, int CT>
+__device__ __forceinline__ void gather_add_pred(float (&acc)[CC], const float* __restrict__ sc, uint32_t idx, int C,
+                                                int ch0) {
+    const uint32_t stride = CT > 0 ? (uint32_t)CT : (uint32_t)C;
+    const float* row = sc + (size_t)idx * stride + ch0;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int q = 0; q < CC / 4; ++q) {
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (idx) v = __ldg(reinterpret_cast<const float4*>(row) + q);
+            acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], v.x);
+            acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], v.y);
+            acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
+            acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], v.w);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < CC; ++c) {
+            float v = 0.0f;
+            if (idx) v = __ldg(row + c);
+            acc[c] = __fadd_rn(acc[c], v);
+        }
+    }
+}
+
+// KIND 0: 27-tap box; 1: cross Laplacian; 2: cross 7-tap sum.  Channels
+// [ch0, ch0+CC) of one voxel whose own brick cell is `cc` in brick `ibk`.
+template <int KIND, int CC, bool VEC, int CT>
 __device__ __forceinline__ void brick_consume(const uint32_t* __restrict__ ibk, int cc, uint32_t index,
                                               const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
+    const int Cs = CT > 0 ? CT : C;
     float acc[CC];
 #pragma unroll
     for (int c = 0; c < CC; ++c) acc[c] = 0.0f;
     if constexpr (KIND == 0) {
 #pragma unroll
-        for (int t = 0; t < kBoxTaps; ++t) {
-            const uint32_t idx = ibk[cc + box_cell_delta(t)];
-            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
-        }
+        for (int t = 0; t < kBoxTaps; ++t) gather_add_pred<CC, VEC, CT>(acc, sc, ibk[cc + box_cell_delta(t)], Cs, ch0);
     } else {
 #pragma unroll
         for (int j = 0; j < kCrossTaps; ++j) {
             if (KIND == 1 && j == 3) continue;  // the Laplacian's centre enters below
-            const uint32_t idx = ibk[cc + cross_cell_delta(j)];
-            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
+            gather_add_pred<CC, VEC, CT>(acc, sc, ibk[cc + cross_cell_delta(j)], Cs, ch0);
         }
         if constexpr (KIND == 1) {
             float v[CC];
-            load_row<CC, VEC>(v, sc, index, C, ch0);
+            load_row<CC, VEC>(v, sc, index, Cs, ch0);
 #pragma unroll
             for (int c = 0; c < CC; ++c) acc[c] = __fsub_rn(acc[c], __fmul_rn(6.0f, v[c]));
         }
     }
-    store_row<CC, VEC>(out, index, C, ch0, acc);
+    store_row<CC, VEC>(out, index, Cs, ch0, acc);
 }
 
 // One-channel consumers reading a value brick (+0.0 in inactive cells; adding
@@ -219,14 +247,14 @@ __device__ __forceinline__ BrickSmem carve(unsigned char* smem, int log2w) {
 // Filter kernel: channels [ch_begin, ch_begin + lanes*CC); `lanes` threads per
 // voxel, each handling CC consecutive channels (VEC: as float4s).  VALUES: one
 // channel, value bricks (lanes == CC == 1).
-template <int KIND, int CC, bool VEC, bool VALUES>
+template <int KIND, int CC, bool VEC, bool VALUES, int CT>
 __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
                                                            float* __restrict__ out, int C, int ch_begin, int lanes) {
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
     brick_prologue(g, k, m.offs, m.lof, m.starts);
-    const uint32_t L = (uint32_t)lanes;
+    const uint32_t L = CT > 0 ? (uint32_t)(CT / CC) : (uint32_t)lanes;
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<VALUES>(g, k, m.offs, m.starts, l0, nb, m.ib, sc);
@@ -241,7 +269,7 @@ __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const floa
             for (uint32_t it = threadIdx.x; it < items; it += blockDim.x) {
                 const uint32_t v = L == 1 ? it : it / L, q = it - v * L, s = sb + v;
                 const uint32_t* ibk = m.ib + (uint32_t)(m.lof[s] - l0) * kCells;
-                brick_consume<KIND, CC, VEC>(ibk, own_cell(m.offs[s]), 1u + k.b * k.W + s, sc, out, C,
+                brick_consume<KIND, CC, VEC, CT>(ibk, own_cell(m.offs[s]), 1u + k.b * k.W + s, sc, out, C,
                                              ch_begin + (int)(q * CC));
             }
         }
@@ -277,9 +305,9 @@ __global__ void __launch_bounds__(512) brick_taps_kernel(DevGrid g, uint32_t* __
     if (blockIdx.x == 0 && threadIdx.x < (unsigned)SHAPE) taps[threadIdx.x] = 0u;
 }
 
-template <int KIND, int CC, bool VEC, bool VALUES>
+template <int KIND, int CC, bool VEC, bool VALUES, int CT = 0>
 cudaError_t launch_brick(const DevGrid& g, const float* sc, int C, int lanes, float* out, cudaStream_t stream) {
-    brick_filter_kernel<KIND, CC, VEC, VALUES>
+    brick_filter_kernel<KIND, CC, VEC, VALUES, CT>
         <<<g.n_blocks, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(g, sc, out, C, 0, lanes);
     return cudaGetLastError();
 }
@@ -292,9 +320,12 @@ constexpr int kVecChannels = 4;
 template <int KIND>
 cudaError_t launch_brick_kind(const DevGrid& g, const float* sc, int C, float* out, cudaStream_t stream) {
     switch (C) {
-        case 1: return launch_brick<KIND, 1, false, true>(g, sc, C, 1, out, stream);
-        case 2: return launch_brick<KIND, 2, false, false>(g, sc, C, 1, out, stream);
-        case 3: return launch_brick<KIND, 3, false, false>(g, sc, C, 1, out, stream);
+        case 1: return launch_brick<KIND, 1, false, true, 1>(g, sc, C, 1, out, stream);
+        case 2: return launch_brick<KIND, 2, false, false, 2>(g, sc, C, 1, out, stream);
+        case 3: return launch_brick<KIND, 3, false, false, 3>(g, sc, C, 1, out, stream);
+        case 4: return launch_brick<KIND, 4, true, false, 4>(g, sc, C, 1, out, stream);
+        case 8: return launch_brick<KIND, 4, true, false, 8>(g, sc, C, 2, out, stream);
+        case 16: return launch_brick<KIND, 4, true, false, 16>(g, sc, C, 4, out, stream);
         default: break;
     }
     if (C % kVecChannels == 0) return launch_brick<KIND, kVecChannels, true, false>(g, sc, C, C / kVecChannels, out, stream);
