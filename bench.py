@@ -312,6 +312,20 @@ def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
                     res.append({"kernel": "box", "W": 1 << log2w, "C": C, "resolver": rname, "output": oname,
                                 "ms": round(ms, 5)})
         g.close()
+    # grid builders (host C++ and GPU), wall time including upload / allocation
+    dcoords = torch.from_numpy(coords).cuda()
+    for name, fn in (("build_host", lambda: vbm.vbm_build(coords, 9)),
+                     ("build_device", lambda: vbm.vbm_build_device(dcoords, 9))):
+        fn().close()
+        ts = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            g = fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+            g.close()
+        res.append({"kernel": name, "W": 512, "ms": round(1e3 * statistics.median(ts), 3)})
     for log2w in (6, 7, 8, 9):
         g = vbm.vbm_build(coords, log2w)
         for rname, r in (("walk", vbm.RESOLVE_TREEWALK), ("cached", vbm.RESOLVE_CACHED),

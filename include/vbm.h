@@ -122,6 +122,19 @@ const char* vbm_last_error(void);
 int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
               vbm_grid** out);
 
+/* Build the same grid from coordinates already in device memory: coords is a
+ * device array of 3n int32 on the current device (any order).  The work runs
+ * on the GPU (leaf hash table, masks by atomic OR, a radix sort of the leaves
+ * into tree order, scans for first indices and node ids, parallel fill of the
+ * leaf records, child tables, VBM block metadata and neighbour rows); the
+ * result equals vbm_build's array for array.  Temporary device memory is
+ * allocated and freed inside the call (about 12 bytes per voxel for the hash
+ * table plus ~150 bytes per leaf); the call synchronises `stream` and also
+ * keeps host copies of the grid's arrays for vbm_leaf_export.  Requires
+ * |x|,|y|,|z| < 2^20 (VBM_ERR_RANGE otherwise).  Errors: as vbm_build. */
+int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
+                     vbm_grid** out);
+
 /* Free a grid and its device arrays.  NULL is accepted.  The caller must make
  * sure no launched work still uses the grid (synchronise its streams first). */
 int vbm_destroy(vbm_grid* grid);

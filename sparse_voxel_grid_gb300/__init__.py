@@ -43,7 +43,7 @@ SENTINEL_LEAF = 0xFFFFFFFF
 SENTINEL_OFFSET = 0xFFFF
 
 __all__ = [
-    "Grid", "VbmError", "vbm_build", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
+    "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
     "vbm_box_filter", "vbm_cross_filter", "vbm_box_taps", "vbm_cross_taps", "vbm_last_error",
 ]
 
@@ -124,6 +124,18 @@ def vbm_build(coords, log2_block_width: int = 7, flags: int = 0, stream=None) ->
     s = ctypes.c_void_p(None) if (flags & BUILD_HOST_ONLY) else _stream_handle(stream)
     check(load().vbm_build(c.ctypes.data if len(c) else None, len(c), int(log2_block_width), int(flags), s,
                            ctypes.byref(h)))
+    return Grid(h.value)
+
+
+def vbm_build_device(coords, log2_block_width: int = 7, flags: int = 0, stream=None) -> Grid:
+    """Build a grid on the GPU from an (N,3) int32 CUDA tensor of coordinates."""
+    import torch
+    if not isinstance(coords, torch.Tensor) or not coords.is_cuda or coords.dtype != torch.int32:
+        raise TypeError("coords must be an int32 CUDA tensor")
+    c = coords.reshape(-1, 3).contiguous()
+    h = ctypes.c_void_p()
+    check(load().vbm_build_device(ctypes.c_void_p(c.data_ptr()) if c.numel() else None, c.shape[0],
+                                  int(log2_block_width), int(flags), _stream_handle(stream), ctypes.byref(h)))
     return Grid(h.value)
 
 

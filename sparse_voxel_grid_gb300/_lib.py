@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH):
             lib.vbm_last_error.argtypes = []
             lib.vbm_build.restype = i32
             lib.vbm_build.argtypes = [p, u64, i32, u32, p, ctypes.POINTER(p)]
+            lib.vbm_build_device.restype = i32
+            lib.vbm_build_device.argtypes = [p, u64, i32, u32, p, ctypes.POINTER(p)]
             lib.vbm_destroy.restype = i32
             lib.vbm_destroy.argtypes = [p]
             lib.vbm_info.restype = i32

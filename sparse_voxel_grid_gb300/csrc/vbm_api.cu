@@ -46,59 +46,32 @@ class DeviceGuard {
 
 // Copies the host arrays into one device allocation and fills g->dev.
 int upload(vbm_grid* g, cudaStream_t stream) {
-    struct Part {
-        const void* src;
-        size_t bytes;
-        size_t off;
-    };
-    Part parts[7] = {
-        {g->leaves.data(), g->leaves.size() * sizeof(vbm::LeafRec), 0},
-        {g->root_keys.data(), g->root_keys.size() * sizeof(uint64_t), 0},
-        {g->upper.data(), g->upper.size() * sizeof(uint32_t), 0},
-        {g->lower.data(), g->lower.size() * sizeof(uint32_t), 0},
-        {g->first_leaf.data(), g->first_leaf.size() * sizeof(uint32_t), 0},
-        {g->jump.data(), g->jump.size() * sizeof(uint64_t), 0},
-        {g->nbr.data(), g->nbr.size() * sizeof(uint32_t), 0},
-    };
-    size_t total = 0;
-    for (Part& p : parts) {
-        p.off = total;
-        total = round_up(total + p.bytes, 256);
-    }
-    total = total ? total : 256;
+    const vbm::ArenaLayout lay = vbm::arena_layout(g->leaves.size(), g->root_keys.size(), g->n_lower,
+                                                   g->first_leaf.size(), g->log2w);
+    const void* src[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
+                          g->first_leaf.data(), g->jump.data(), g->nbr.data()};
     cudaError_t e = cudaGetDevice(&g->device);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaGetDevice", e);
-    e = cudaMalloc(&g->arena, total);
+    int sm_count = 0;
+    e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, g->device);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: cudaDeviceGetAttribute", e);
+    e = cudaMalloc(&g->arena, lay.total);
     if (e != cudaSuccess) {
         g->arena = nullptr;
         cudaGetLastError();
-        return fail(VBM_ERR_NOMEM, std::string("vbm_build: cudaMalloc of ") + std::to_string(total) +
+        return fail(VBM_ERR_NOMEM, std::string("vbm_build: cudaMalloc of ") + std::to_string(lay.total) +
                                        " bytes failed: " + cudaGetErrorString(e));
     }
-    g->arena_bytes = total;
+    g->arena_bytes = lay.total;
     char* base = static_cast<char*>(g->arena);
-    for (const Part& p : parts) {
-        if (!p.bytes) continue;
-        e = cudaMemcpyAsync(base + p.off, p.src, p.bytes, cudaMemcpyHostToDevice, stream);
+    for (int i = 0; i < 7; ++i) {
+        if (!lay.bytes[i]) continue;
+        e = cudaMemcpyAsync(base + lay.off[i], src[i], lay.bytes[i], cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return fail_cuda("vbm_build: cudaMemcpyAsync", e);
     }
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);
-    vbm::DevGrid& d = g->dev;
-    d.leaves = reinterpret_cast<const vbm::LeafRec*>(base + parts[0].off);
-    d.root_keys = reinterpret_cast<const uint64_t*>(base + parts[1].off);
-    d.upper = reinterpret_cast<const uint32_t*>(base + parts[2].off);
-    d.lower = reinterpret_cast<const uint32_t*>(base + parts[3].off);
-    d.first_leaf = reinterpret_cast<const uint32_t*>(base + parts[4].off);
-    d.jump = reinterpret_cast<const uint64_t*>(base + parts[5].off);
-    d.nbr = reinterpret_cast<const uint32_t*>(base + parts[6].off);
-    d.n = (uint32_t)g->n;
-    d.n_leaves = (uint32_t)g->n_leaves;
-    d.n_blocks = (uint32_t)g->n_blocks;
-    d.n_upper = g->n_upper;
-    d.log2w = g->log2w;
-    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, g->device);
-    if (e != cudaSuccess) return fail_cuda("vbm_build: cudaDeviceGetAttribute", e);
+    vbm::set_device_views(g, lay, sm_count);
     return VBM_OK;
 }
 
@@ -151,6 +124,33 @@ int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t 
             vbm_destroy(g);
             return fail(rc, msg);
         }
+    }
+    *out = g;
+    return VBM_OK;
+}
+
+int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
+                     vbm_grid** out) {
+    g_last_error.clear();
+    if (!out) return fail(VBM_ERR_INVALID, "vbm_build_device: out is NULL");
+    *out = nullptr;
+    if (!coords && n) return fail(VBM_ERR_INVALID, "vbm_build_device: coords is NULL");
+    if (log2_block_width < 6 || log2_block_width > 9)
+        return fail(VBM_ERR_INVALID, "vbm_build_device: log2_block_width must be in 6..9");
+    if (flags & ~VBM_BUILD_DEDUP) return fail(VBM_ERR_INVALID, "vbm_build_device: unknown flags");
+    vbm_grid* g = new (std::nothrow) vbm_grid;
+    if (!g) return fail(VBM_ERR_NOMEM, "vbm_build_device: out of host memory");
+    int rc;
+    try {
+        std::string err;
+        rc = vbm::build_device(coords, n, log2_block_width, flags, stream, g, err);
+        if (rc != VBM_OK) {
+            vbm_destroy(g);
+            return fail(rc, err);
+        }
+    } catch (const std::bad_alloc&) {
+        vbm_destroy(g);
+        return fail(VBM_ERR_NOMEM, "vbm_build_device: out of host memory");
     }
     *out = g;
     return VBM_OK;

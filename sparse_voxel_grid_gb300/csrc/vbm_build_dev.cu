@@ -1,0 +1,447 @@
+// Device-side index-grid and VBM-metadata builder (vbm_build_device).
+//
+// Produces exactly the arrays of the host builder (vbm_build.cpp) from
+// coordinates already in device memory, without sorting the voxels:
+//   1. leaf origins are inserted into an open-addressing hash table
+//      (atomicCAS on 64-bit packed keys) and the occupied slots compacted into
+//      provisional leaf ids;
+//   2. every voxel sets its bit in its leaf's mask with a 64-bit atomicOr (the
+//      returned old word detects duplicates);
+//   3. the leaves (not the voxels) are put in depth-first tree order by a
+//      stable LSD radix sort of their 54-bit tree keys;
+//   4. scans give each leaf's first index and the upper/lower node ids;
+//   5. leaf records, child tables, VBM block metadata (firstLeafID, jumpMap)
+//      and neighbour rows are filled by one thread per leaf (or per block).
+// Temporary device memory is allocated here and freed before returning.
+// Coordinates must satisfy |x|,|y|,|z| < 2^20 so that leaf keys fit 54 bits.
+#include <cuda_runtime.h>
+
+#include <string>
+#include <vector>
+
+#include "vbm_internal.h"
+#include "vbm_sort.cuh"
+
+namespace vbm {
+namespace {
+
+constexpr uint64_t kEmptyKey = ~0ull;
+constexpr int32_t kDevCoordLimit = 1 << 20;
+constexpr int kThreads = 256;
+constexpr uint32_t kBias18 = 1u << 17;  // leaf coordinate (x>>3) + 2^17 fits 18 bits
+constexpr uint32_t kBias9 = 1u << 8;    // upper coordinate (x>>12) + 2^8 fits 9 bits
+
+__device__ __forceinline__ uint64_t pack_leaf(int32_t lx, int32_t ly, int32_t lz) {  // lx = x >> 3
+    return ((uint64_t)(uint32_t)(lx + (int32_t)kBias18) << 36) | ((uint64_t)(uint32_t)(ly + (int32_t)kBias18) << 18) |
+           (uint64_t)(uint32_t)(lz + (int32_t)kBias18);
+}
+__device__ __forceinline__ void unpack_leaf(uint64_t k, int32_t& lx, int32_t& ly, int32_t& lz) {
+    lx = (int32_t)((k >> 36) & 0x3FFFFu) - (int32_t)kBias18;
+    ly = (int32_t)((k >> 18) & 0x3FFFFu) - (int32_t)kBias18;
+    lz = (int32_t)(k & 0x3FFFFu) - (int32_t)kBias18;
+}
+
+// Tree key of a leaf (origin = 8*(lx,ly,lz)): biased upper coordinates (9 bits
+// each), then the lower slot (15 bits), then the leaf slot (12 bits).
+// Unsigned order = the builder's depth-first order.
+__device__ __forceinline__ uint64_t tree_key(int32_t lx, int32_t ly, int32_t lz) {
+    const int32_t x = lx * 8, y = ly * 8, z = lz * 8;
+    const uint64_t up = ((uint64_t)(uint32_t)((x >> 12) + (int32_t)kBias9) << 18) |
+                        ((uint64_t)(uint32_t)((y >> 12) + (int32_t)kBias9) << 9) |
+                        (uint64_t)(uint32_t)((z >> 12) + (int32_t)kBias9);
+    const uint64_t lower = (uint64_t)(((x >> 7) & 31) << 10 | ((y >> 7) & 31) << 5 | ((z >> 7) & 31));
+    const uint64_t leaf = (uint64_t)(((x >> 3) & 15) << 8 | ((y >> 3) & 15) << 4 | ((z >> 3) & 15));
+    return (up << 27) | (lower << 12) | leaf;
+}
+
+__device__ __forceinline__ uint64_t mix64d(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+// Slot of `key` in the table (inserting it when `insert`); the table always
+// has an empty slot, so the probe ends; `cap` bounds it regardless.
+__device__ __forceinline__ int64_t probe(uint64_t* keys, uint64_t mask, uint64_t key, bool insert) {
+    uint64_t slot = mix64d(key) & mask;
+    for (uint64_t it = 0; it <= mask; ++it) {
+        const uint64_t cur = insert ? atomicCAS((unsigned long long*)&keys[slot], (unsigned long long)kEmptyKey,
+                                                (unsigned long long)key)
+                                    : keys[slot];
+        if (cur == key || (insert && cur == kEmptyKey)) return (int64_t)slot;
+        if (!insert && cur == kEmptyKey) return -1;
+        slot = (slot + 1) & mask;
+    }
+    return -1;
+}
+
+// 1. Insert leaf keys; flag coordinates out of range.
+__global__ void insert_kernel(const int32_t* __restrict__ coords, uint64_t n, uint64_t* keys, uint64_t mask,
+                              uint32_t* __restrict__ err) {
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        const int32_t x = coords[3 * i], y = coords[3 * i + 1], z = coords[3 * i + 2];
+        if (x <= -kDevCoordLimit || x >= kDevCoordLimit || y <= -kDevCoordLimit || y >= kDevCoordLimit ||
+            z <= -kDevCoordLimit || z >= kDevCoordLimit) {
+            atomicOr(err, 1u);
+            continue;
+        }
+        if (probe(keys, mask, pack_leaf(x >> 3, y >> 3, z >> 3), true) < 0) atomicOr(err, 2u);
+    }
+}
+
+// 2. Compact occupied slots into provisional leaf ids (arbitrary order).
+__global__ void compact_kernel(const uint64_t* __restrict__ keys, uint64_t cap, uint32_t* __restrict__ slot_id,
+                               uint32_t* __restrict__ counter, uint64_t* __restrict__ tkey, uint32_t* __restrict__ tval,
+                               uint64_t* __restrict__ pkey) {
+    for (uint64_t s = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; s < cap; s += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t k = keys[s];
+        if (k == kEmptyKey) continue;
+        const uint32_t id = atomicAdd(counter, 1u);
+        slot_id[s] = id;
+        int32_t lx, ly, lz;
+        unpack_leaf(k, lx, ly, lz);
+        tkey[id] = tree_key(lx, ly, lz);
+        tval[id] = id;
+        pkey[id] = k;
+    }
+}
+
+// 3. Set each voxel's bit in its provisional leaf's mask; count repeats.
+__global__ void mask_kernel(const int32_t* __restrict__ coords, uint64_t n, uint64_t* keys, uint64_t mask,
+                            const uint32_t* __restrict__ slot_id, unsigned long long* __restrict__ tmask,
+                            uint32_t* __restrict__ dups) {
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        const int32_t x = coords[3 * i], y = coords[3 * i + 1], z = coords[3 * i + 2];
+        const int64_t slot = probe(keys, mask, pack_leaf(x >> 3, y >> 3, z >> 3), false);
+        if (slot < 0) continue;  // reported by insert_kernel
+        const uint32_t off = (uint32_t)((x & 7) << 6 | (y & 7) << 3 | (z & 7));
+        const unsigned long long bit = 1ull << (off & 63u);
+        const unsigned long long old = atomicOr(&tmask[(size_t)slot_id[slot] * 8u + (off >> 6)], bit);
+        if (old & bit) atomicAdd(dups, 1u);
+    }
+}
+
+// 4. Per final leaf: popcount of its mask (input of the first-index scan) and
+// the inverse permutation.
+__global__ void count_kernel(const uint32_t* __restrict__ perm, uint32_t nl, const unsigned long long* __restrict__ tmask,
+                             uint32_t* __restrict__ cnt, uint32_t* __restrict__ final_of) {
+    for (uint32_t L = blockIdx.x * blockDim.x + threadIdx.x; L < nl; L += gridDim.x * blockDim.x) {
+        const uint32_t t = perm[L];
+        uint32_t c = 0;
+        for (int w = 0; w < 8; ++w) c += (uint32_t)__popcll(tmask[(size_t)t * 8u + w]);
+        cnt[L] = c;
+        final_of[t] = L;
+    }
+}
+
+// Node-boundary flags on the sorted tree keys: upper node changes / lower node changes.
+__global__ void node_flag_kernel(const uint64_t* __restrict__ skey, uint32_t nl, uint32_t* __restrict__ up_flag,
+                                 uint32_t* __restrict__ lo_flag) {
+    for (uint32_t L = blockIdx.x * blockDim.x + threadIdx.x; L < nl; L += gridDim.x * blockDim.x) {
+        const uint64_t k = skey[L];
+        const bool nu = L == 0 || (skey[L - 1] >> 27) != (k >> 27);
+        const bool nlw = L == 0 || (skey[L - 1] >> 12) != (k >> 12);
+        up_flag[L] = nu ? 1u : 0u;
+        lo_flag[L] = nlw ? 1u : 0u;
+    }
+}
+
+__global__ void count_occupied_kernel(const uint64_t* __restrict__ keys, uint64_t cap, uint32_t* __restrict__ counter) {
+    uint32_t c = 0;
+    for (uint64_t s = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; s < cap; s += (uint64_t)gridDim.x * blockDim.x)
+        c += keys[s] != kEmptyKey;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if ((threadIdx.x & 31u) == 0 && c) atomicAdd(counter, c);
+}
+
+// 5a. Leaf records in tree order: masks, 9-bit directory, per-word bases, first
+// index (1 + exclusive scan of the counts), origin.
+__global__ void leafrec_kernel(const uint32_t* __restrict__ perm, uint32_t nl, const unsigned long long* __restrict__ tmask,
+                               const uint32_t* __restrict__ cnt_ex, const uint64_t* __restrict__ pkey,
+                               LeafRec* __restrict__ leaves) {
+    for (uint32_t L = blockIdx.x * blockDim.x + threadIdx.x; L < nl; L += gridDim.x * blockDim.x) {
+        const uint32_t t = perm[L];
+        LeafRec r;
+        const uint32_t first = 1u + cnt_ex[L];
+        uint32_t run = 0;
+        r.prefix = 0;
+        for (int w = 0; w < 8; ++w) {
+            r.mask[w] = tmask[(size_t)t * 8u + w];
+            if (w >= 1) r.prefix |= (uint64_t)run << (9 * (w - 1));
+            r.base[w] = first + run;
+            run += (uint32_t)__popcll(r.mask[w]);
+        }
+        r.first = first;
+        r.count = run;
+        int32_t lx, ly, lz;
+        unpack_leaf(pkey[t], lx, ly, lz);
+        r.origin[0] = lx * 8;
+        r.origin[1] = ly * 8;
+        r.origin[2] = lz * 8;
+        r.pad = 0;
+        leaves[L] = r;
+    }
+}
+
+// 5b. Root keys and dense child tables.  up_ex/lo_ex: exclusive scans of the
+// node-boundary flags over the sorted tree keys.
+__global__ void tables_kernel(const uint64_t* __restrict__ skey, uint32_t nl, const uint32_t* __restrict__ up_ex,
+                              const uint32_t* __restrict__ lo_ex, const LeafRec* __restrict__ leaves,
+                              uint64_t* __restrict__ root_keys, uint32_t* __restrict__ upper, uint32_t* __restrict__ lower) {
+    for (uint32_t L = blockIdx.x * blockDim.x + threadIdx.x; L < nl; L += gridDim.x * blockDim.x) {
+        const uint64_t k = skey[L];
+        const bool nu = L == 0 || (skey[L - 1] >> 27) != (k >> 27);
+        const bool nlw = L == 0 || (skey[L - 1] >> 12) != (k >> 12);
+        const uint32_t uid = up_ex[L] + (nu ? 1u : 0u) - 1u;
+        const uint32_t lid = lo_ex[L] + (nlw ? 1u : 0u) - 1u;
+        const int32_t x = leaves[L].origin[0], y = leaves[L].origin[1], z = leaves[L].origin[2];
+        if (nu) root_keys[uid] = root_key_of(x, y, z);
+        if (nlw) upper[(size_t)uid * kUpperSlots + (uint32_t)((k >> 12) & 32767u)] = lid;
+        lower[(size_t)lid * kLowerSlots + (uint32_t)(k & 4095u)] = L;
+    }
+}
+
+// 5c. VBM blocks: firstLeafID of every block starting inside leaf L; the
+// jumpMap bit of L's first index unless it starts a block.
+__global__ void blocks_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, int log2w, uint32_t* __restrict__ first_leaf,
+                              unsigned long long* __restrict__ jump) {
+    const uint32_t W = 1u << log2w, words = W >> 6;
+    for (uint32_t L = blockIdx.x * blockDim.x + threadIdx.x; L < nl; L += gridDim.x * blockDim.x) {
+        const uint32_t f = leaves[L].first, c = leaves[L].count;  // indices f .. f+c-1
+        for (uint32_t b = (f - 1u + W - 1u) >> log2w; (b << log2w) + 1u <= f + c - 1u; ++b) first_leaf[b] = L;
+        const uint32_t b = (f - 1u) >> log2w, s = (f - 1u) & (W - 1u);
+        if (L > 0 && s != 0) atomicOr(&jump[(size_t)b * words + (s >> 6)], 1ull << (s & 63u));
+    }
+}
+
+// 5d. Neighbour rows: leaf at origin + 8*(dx,dy,dz), through the hash table.
+__global__ void nbr_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, uint64_t* keys, uint64_t mask,
+                           const uint32_t* __restrict__ slot_id, const uint32_t* __restrict__ final_of,
+                           uint32_t* __restrict__ nbr) {
+    const uint64_t total = (uint64_t)nl * kNbrStride;
+    for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < total; e += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t L = (uint32_t)(e / kNbrStride), t = (uint32_t)(e % kNbrStride);
+        uint32_t id = kNone;
+        if (t < 27u) {
+            const int32_t lx = (leaves[L].origin[0] >> 3) + (int32_t)(t / 9u) - 1;
+            const int32_t ly = (leaves[L].origin[1] >> 3) + (int32_t)((t / 3u) % 3u) - 1;
+            const int32_t lz = (leaves[L].origin[2] >> 3) + (int32_t)(t % 3u) - 1;
+            const int32_t lim = (int32_t)kBias18;
+            if (lx >= -lim && lx < lim && ly >= -lim && ly < lim && lz >= -lim && lz < lim) {
+                const int64_t slot = probe(keys, mask, pack_leaf(lx, ly, lz), false);
+                if (slot >= 0) id = final_of[slot_id[slot]];
+            }
+        }
+        nbr[e] = id;
+    }
+}
+
+// 5e. Spans: max and the number of blocks over MaxCachedLeaves.
+__global__ void span_kernel(const unsigned long long* __restrict__ jump, uint32_t n_blocks, uint32_t words,
+                            uint32_t* __restrict__ out) {
+    for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < n_blocks; b += gridDim.x * blockDim.x) {
+        uint32_t span = 1;
+        for (uint32_t w = 0; w < words; ++w) span += (uint32_t)__popcll(jump[(size_t)b * words + w]);
+        atomicMax(&out[0], span);
+        if (span > VBM_MAX_CACHED_LEAVES) atomicAdd(&out[1], 1u);
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// Device allocations freed on scope exit.
+struct Scratch {
+    std::vector<void*> ptrs;
+    ~Scratch() {
+        for (void* p : ptrs) cudaFree(p);
+    }
+    template <typename T>
+    cudaError_t alloc(T** p, size_t count) {
+        void* q = nullptr;
+        const cudaError_t e = cudaMalloc(&q, count ? count * sizeof(T) : sizeof(T));
+        if (e == cudaSuccess) ptrs.push_back(q);
+        *p = static_cast<T*>(q);
+        return e;
+    }
+};
+
+unsigned grid_for(uint64_t work, int sm_count) {
+    const uint64_t want = (work + kThreads - 1) / kThreads;
+    const uint64_t cap = (uint64_t)(sm_count > 0 ? sm_count : 1) * 32u;
+    return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+// Stable radix sort of (key, value) pairs by the low `bits` bits of the keys;
+// the result ends in (k0, v0).
+cudaError_t radix_sort(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* v1, uint32_t* hist, uint32_t n, int bits,
+                       cudaStream_t s) {
+    const uint32_t tiles = (n + devsort::kSortThreads - 1) / devsort::kSortThreads;
+    for (int shift = 0; shift < bits; shift += 8) {
+        devsort::radix_hist_kernel<<<tiles, devsort::kSortThreads, 0, s>>>(k0, n, shift, tiles, hist);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, s>>>(hist, (uint64_t)tiles * devsort::kDigits,
+                                                                          nullptr);
+        devsort::radix_scatter_kernel<<<tiles, devsort::kSortThreads, 0, s>>>(k0, v0, k1, v1, n, shift, tiles, hist);
+        std::swap(k0, k1);
+        std::swap(v0, v1);
+    }
+    // An odd number of passes leaves the result in the second buffers.
+    if (((bits + 7) / 8) & 1) {
+        cudaMemcpyAsync(k1, k0, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToDevice, s);
+        cudaMemcpyAsync(v1, v0, (size_t)n * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t read_back(T* host, const T* dev, size_t count, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(host, dev, count * sizeof(T), cudaMemcpyDeviceToHost, s);
+    return e != cudaSuccess ? e : cudaStreamSynchronize(s);
+}
+
+}  // namespace
+
+int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* stream_v, vbm_grid* g,
+                 std::string& err) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+#define VBM_CK(call)                                                                              \
+    do {                                                                                          \
+        const cudaError_t e_ = (call);                                                            \
+        if (e_ != cudaSuccess) {                                                                  \
+            cudaGetLastError();                                                                   \
+            err = std::string("vbm_build_device: ") + #call + ": " + cudaGetErrorString(e_);      \
+            return e_ == cudaErrorMemoryAllocation ? VBM_ERR_NOMEM : VBM_ERR_CUDA;                \
+        }                                                                                         \
+    } while (0)
+    if (n >= (uint64_t)1 << 31) {
+        err = "vbm_build_device: N must be < 2^31";
+        return VBM_ERR_RANGE;
+    }
+    int device = 0, sm = 1;
+    VBM_CK(cudaGetDevice(&device));
+    VBM_CK(cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device));
+    const uint32_t W = 1u << log2w, words = W >> 6;
+    Scratch sc;
+
+    // 1-2. Leaf hash table (capacity a power of two >= 2n) and compaction.
+    uint64_t cap = 1024;
+    while (cap < 2 * n) cap <<= 1;
+    uint64_t* keys;
+    uint32_t *slot_id, *ctr;  // ctr: [0] error flags, [1] leaves, [2] repeats, [3..4] span stats, [5..7] totals
+    VBM_CK(sc.alloc(&keys, cap));
+    VBM_CK(sc.alloc(&slot_id, cap));
+    VBM_CK(sc.alloc(&ctr, 8));
+    VBM_CK(cudaMemsetAsync(keys, 0xFF, cap * sizeof(uint64_t), st));
+    VBM_CK(cudaMemsetAsync(ctr, 0, 8 * sizeof(uint32_t), st));
+    if (n) insert_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, ctr);
+    count_occupied_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, ctr + 1);
+    VBM_CK(cudaGetLastError());
+    uint32_t h[2];
+    VBM_CK(read_back(h, ctr, 2, st));
+    if (h[0] & 1u) {
+        err = "vbm_build_device: a coordinate is outside (-2^20, 2^20)";
+        return VBM_ERR_RANGE;
+    }
+    if (h[0] & 2u) {
+        err = "vbm_build_device: hash table overflow";
+        return VBM_ERR_CUDA;
+    }
+    const uint32_t nl = h[1];
+    uint64_t *tkey, *tkey2, *pkey;
+    uint32_t *tval, *tval2, *hist, *cnt, *final_of, *up_f, *lo_f;
+    unsigned long long* tmask;
+    const uint32_t tiles = (nl + devsort::kSortThreads - 1) / devsort::kSortThreads;
+    VBM_CK(sc.alloc(&tkey, nl));
+    VBM_CK(sc.alloc(&tkey2, nl));
+    VBM_CK(sc.alloc(&pkey, nl));
+    VBM_CK(sc.alloc(&tval, nl));
+    VBM_CK(sc.alloc(&tval2, nl));
+    VBM_CK(sc.alloc(&hist, (size_t)tiles * devsort::kDigits));
+    VBM_CK(sc.alloc(&cnt, nl));
+    VBM_CK(sc.alloc(&final_of, nl));
+    VBM_CK(sc.alloc(&up_f, nl));
+    VBM_CK(sc.alloc(&lo_f, nl));
+    VBM_CK(sc.alloc(&tmask, (size_t)nl * 8u));
+    VBM_CK(cudaMemsetAsync(ctr + 1, 0, sizeof(uint32_t), st));
+    VBM_CK(cudaMemsetAsync(tmask, 0, (size_t)nl * 8u * sizeof(uint64_t), st));
+    compact_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, slot_id, ctr + 1, tkey, tval, pkey);
+    // 3. Masks and repeats.
+    if (n) mask_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, slot_id, tmask, ctr + 2);
+    VBM_CK(cudaGetLastError());
+    uint32_t dups = 0;
+    VBM_CK(read_back(&dups, ctr + 2, 1, st));
+    if (dups && !(flags & VBM_BUILD_DEDUP)) {
+        err = "vbm_build_device: duplicate coordinates (" + std::to_string(dups) + " repeats)";
+        return VBM_ERR_DUPLICATE;
+    }
+    // 4. Tree order of the leaves; counts, first indices, node ids.
+    if (nl) {
+        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, nl, 54, st));
+        count_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, final_of);
+        node_flag_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(cnt, nl, ctr + 5);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(up_f, nl, ctr + 6);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(lo_f, nl, ctr + 7);
+        VBM_CK(cudaGetLastError());
+    }
+    uint32_t tot[3] = {0, 0, 0};
+    if (nl) VBM_CK(read_back(tot, ctr + 5, 3, st));
+    const uint64_t N = tot[0];
+    g->n = N;
+    g->log2w = log2w;
+    g->n_leaves = nl;
+    g->n_upper = tot[1];
+    g->n_lower = tot[2];
+    g->n_blocks = (N + W - 1) / W;
+    g->device = device;
+
+    // 5. The grid's arena, laid out as vbm_build's.
+    const ArenaLayout lay = arena_layout(nl, g->n_upper, g->n_lower, g->n_blocks, log2w);
+    VBM_CK(cudaMalloc(&g->arena, lay.total));
+    g->arena_bytes = lay.total;
+    char* base = static_cast<char*>(g->arena);
+    LeafRec* leaves = reinterpret_cast<LeafRec*>(base + lay.off[0]);
+    uint64_t* root_keys = reinterpret_cast<uint64_t*>(base + lay.off[1]);
+    uint32_t* upper = reinterpret_cast<uint32_t*>(base + lay.off[2]);
+    uint32_t* lower = reinterpret_cast<uint32_t*>(base + lay.off[3]);
+    uint32_t* first_leaf = reinterpret_cast<uint32_t*>(base + lay.off[4]);
+    unsigned long long* jump = reinterpret_cast<unsigned long long*>(base + lay.off[5]);
+    uint32_t* nbr = reinterpret_cast<uint32_t*>(base + lay.off[6]);
+    VBM_CK(cudaMemsetAsync(upper, 0xFF, lay.bytes[2], st));
+    VBM_CK(cudaMemsetAsync(lower, 0xFF, lay.bytes[3], st));
+    VBM_CK(cudaMemsetAsync(jump, 0, lay.bytes[5], st));
+    VBM_CK(cudaMemsetAsync(ctr + 3, 0, 2 * sizeof(uint32_t), st));
+    if (nl) {
+        leafrec_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, pkey, leaves);
+        tables_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f, leaves, root_keys, upper, lower);
+        blocks_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(leaves, nl, log2w, first_leaf, jump);
+        nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
+                                                                                 final_of, nbr);
+        span_kernel<<<grid_for(g->n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)g->n_blocks, words, ctr + 3);
+        VBM_CK(cudaGetLastError());
+    }
+    uint32_t spans[2] = {0, 0};
+    VBM_CK(read_back(spans, ctr + 3, 2, st));
+    g->max_span = spans[0];
+    g->n_over_cache = spans[1];
+    set_device_views(g, lay, sm);
+
+    // Host mirrors (vbm_info, vbm_leaf_export).
+    g->leaves.resize(nl);
+    g->root_keys.resize(g->n_upper);
+    g->upper.resize((size_t)g->n_upper * kUpperSlots);
+    g->lower.resize((size_t)g->n_lower * kLowerSlots);
+    g->first_leaf.resize(g->n_blocks);
+    g->jump.resize(g->n_blocks * words);
+    g->nbr.resize((size_t)nl * kNbrStride);
+    void* dst[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
+                    g->first_leaf.data(), g->jump.data(), g->nbr.data()};
+    for (int i = 0; i < 7; ++i)
+        if (lay.bytes[i]) VBM_CK(cudaMemcpyAsync(dst[i], base + lay.off[i], lay.bytes[i], cudaMemcpyDeviceToHost, st));
+    VBM_CK(cudaStreamSynchronize(st));
+#undef VBM_CK
+    return VBM_OK;
+}
+
+}  // namespace vbm

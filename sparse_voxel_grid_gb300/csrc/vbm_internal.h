@@ -95,7 +95,59 @@ struct vbm_grid {
 };
 
 namespace vbm {
+
+// Byte offsets of the grid's arrays in its one device allocation, in the order
+// leaves, root_keys, upper, lower, first_leaf, jump, nbr (256-byte aligned).
+struct ArenaLayout {
+    size_t off[7];
+    size_t bytes[7];
+    size_t total;
+};
+
+inline ArenaLayout arena_layout(size_t n_leaves, size_t n_upper, size_t n_lower, size_t n_blocks, int log2w) {
+    ArenaLayout a;
+    const size_t words = ((size_t)1 << log2w) / 64;
+    a.bytes[0] = n_leaves * sizeof(LeafRec);
+    a.bytes[1] = n_upper * sizeof(uint64_t);
+    a.bytes[2] = n_upper * (size_t)kUpperSlots * sizeof(uint32_t);
+    a.bytes[3] = n_lower * (size_t)kLowerSlots * sizeof(uint32_t);
+    a.bytes[4] = n_blocks * sizeof(uint32_t);
+    a.bytes[5] = n_blocks * words * sizeof(uint64_t);
+    a.bytes[6] = n_leaves * (size_t)kNbrStride * sizeof(uint32_t);
+    size_t total = 0;
+    for (int i = 0; i < 7; ++i) {
+        a.off[i] = total;
+        total = (total + a.bytes[i] + 255) / 256 * 256;
+    }
+    a.total = total ? total : 256;
+    return a;
+}
+
+// Device views of an arena laid out by arena_layout (sizes from g).
+inline void set_device_views(vbm_grid* g, const ArenaLayout& a, int sm_count) {
+    char* base = static_cast<char*>(g->arena);
+    DevGrid& d = g->dev;
+    d.leaves = reinterpret_cast<const LeafRec*>(base + a.off[0]);
+    d.root_keys = reinterpret_cast<const uint64_t*>(base + a.off[1]);
+    d.upper = reinterpret_cast<const uint32_t*>(base + a.off[2]);
+    d.lower = reinterpret_cast<const uint32_t*>(base + a.off[3]);
+    d.first_leaf = reinterpret_cast<const uint32_t*>(base + a.off[4]);
+    d.jump = reinterpret_cast<const uint64_t*>(base + a.off[5]);
+    d.nbr = reinterpret_cast<const uint32_t*>(base + a.off[6]);
+    d.n = (uint32_t)g->n;
+    d.n_leaves = (uint32_t)g->n_leaves;
+    d.n_blocks = (uint32_t)g->n_blocks;
+    d.n_upper = g->n_upper;
+    d.log2w = g->log2w;
+    d.sm_count = sm_count;
+}
+
 // Host builder (vbm_build.cpp).  Fills every host array of g; returns a status
 // code and sets err on failure.
 int build_host(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, vbm_grid* g, std::string& err);
+
+// Device builder (vbm_build_dev.cu): coords is a device array of 3n int32.
+// Fills the device arena and the host mirrors of g; synchronises `stream`.
+int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* stream, vbm_grid* g,
+                 std::string& err);
 }  // namespace vbm
