@@ -135,6 +135,35 @@ int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t 
 int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
                      vbm_grid** out);
 
+/* vbm_build_device without any device allocation.  No counterpart on the
+ * pages: this is a library-level variant for callers that cannot call
+ * cudaMalloc -- code that must run while other work is being captured into a
+ * CUDA graph, or that lives inside an application whose device memory is
+ * managed by an allocator it does not own.  Such a caller passes, besides the
+ * coordinates (device array of 3n int32), the output memory: `arena`, a
+ * 256-byte aligned device buffer of `arena_bytes` bytes that receives the
+ * grid's arrays.
+ *   - Temporary memory is a file-scope static device array of about 9.2 MB,
+ *     sized for at most 65,536 voxels; every GPU that loads libvbm.so holds it
+ *     until the process exits.  Larger inputs fail with VBM_ERR_RANGE.
+ *   - If `arena` is NULL or too small the call fails with VBM_ERR_RANGE; when
+ *     `arena_needed` is not NULL it receives the bytes this grid needs (so a
+ *     first call with arena_bytes = 0 is a size query).
+ *   - The first call on each device looks up the static array's address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same static array, which keeps the previous call's
+ *     contents (the call clears what must start empty).  Calls that overlap
+ *     on the GPU -- on different streams or host threads -- race; serialise
+ *     them.
+ *   - The call synchronises `stream`.  The handle owns no device memory:
+ *     vbm_destroy frees only the handle, and the caller frees `arena` after
+ *     destroying it.  The handle keeps no host copies (vbm_leaf_export returns
+ *     VBM_ERR_STATE); every compute call works on it as on any grid.
+ * Requires |x|,|y|,|z| < 2^20.  Errors: INVALID, ALIGN, RANGE, DUPLICATE, CUDA. */
+int vbm_build_device_noalloc(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* arena,
+                             uint64_t arena_bytes, uint64_t* arena_needed, void* stream, vbm_grid** out);
+
 /* Free a grid and its device arrays.  NULL is accepted.  The caller must make
  * sure no launched work still uses the grid (synchronise its streams first). */
 int vbm_destroy(vbm_grid* grid);

@@ -70,6 +70,9 @@ def load(path: str = LIB_PATH):
             lib.vbm_build.argtypes = [p, u64, i32, u32, p, ctypes.POINTER(p)]
             lib.vbm_build_device.restype = i32
             lib.vbm_build_device.argtypes = [p, u64, i32, u32, p, ctypes.POINTER(p)]
+            lib.vbm_build_device_noalloc.restype = i32
+            lib.vbm_build_device_noalloc.argtypes = [p, u64, i32, u32, p, u64, ctypes.POINTER(u64), p,
+                                                     ctypes.POINTER(p)]
             lib.vbm_destroy.restype = i32
             lib.vbm_destroy.argtypes = [p]
             lib.vbm_info.restype = i32

@@ -156,11 +156,34 @@ int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, ui
     return VBM_OK;
 }
 
+int vbm_build_device_noalloc(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* arena,
+                             uint64_t arena_bytes, uint64_t* arena_needed, void* stream, vbm_grid** out) {
+    g_last_error.clear();
+    if (arena_needed) *arena_needed = 0;
+    if (!out) return fail(VBM_ERR_INVALID, "vbm_build_device_noalloc: out is NULL");
+    *out = nullptr;
+    if (!coords && n) return fail(VBM_ERR_INVALID, "vbm_build_device_noalloc: coords is NULL");
+    if (log2_block_width < 6 || log2_block_width > 9)
+        return fail(VBM_ERR_INVALID, "vbm_build_device_noalloc: log2_block_width must be in 6..9");
+    if (flags & ~VBM_BUILD_DEDUP) return fail(VBM_ERR_INVALID, "vbm_build_device_noalloc: unknown flags");
+    vbm_grid* g = new (std::nothrow) vbm_grid;
+    if (!g) return fail(VBM_ERR_NOMEM, "vbm_build_device_noalloc: out of host memory");
+    std::string err;
+    const int rc = vbm::build_device_noalloc(coords, n, log2_block_width, flags, arena, arena_bytes, arena_needed,
+                                             stream, g, err);
+    if (rc != VBM_OK) {
+        delete g;  // owns no device memory
+        return fail(rc, err);
+    }
+    *out = g;
+    return VBM_OK;
+}
+
 int vbm_destroy(vbm_grid* g) {
     g_last_error.clear();
     if (!g) return VBM_OK;
     int rc = VBM_OK;
-    if (g->arena) {
+    if (g->arena && g->owns_arena) {
         DeviceGuard guard(g->device);
         cudaError_t e = cudaFree(g->arena);
         if (e != cudaSuccess) rc = fail_cuda("vbm_destroy: cudaFree", e);
@@ -190,6 +213,7 @@ int vbm_info(const vbm_grid* g, vbm_info_t* info) {
 int vbm_leaf_export(const vbm_grid* g, int what, void* dst, uint64_t bytes) {
     g_last_error.clear();
     if (!g || (!dst && bytes)) return fail(VBM_ERR_INVALID, "vbm_leaf_export: NULL argument");
+    if (!g->host_mirrors) return fail(VBM_ERR_STATE, "vbm_leaf_export: this grid keeps no host copies");
     const size_t nl = g->leaves.size();
     size_t need = 0;
     switch (what) {

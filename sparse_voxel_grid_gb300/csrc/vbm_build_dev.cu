@@ -444,4 +444,201 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     return VBM_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  For callers that cannot call cudaMalloc: all
+// temporary memory lives in one file-scope static device array, sized for at
+// most kNoAllocMaxVoxels voxels, and the grid's arrays go into the caller's
+// buffer.  Every GPU that loads the library holds the static array until the
+// process exits.  Calls share it, so calls that overlap on the GPU race.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr uint64_t kNoAllocMaxVoxels = 65536;  // also the most leaves
+constexpr uint64_t kNoAllocCap = 2 * kNoAllocMaxVoxels;  // hash capacity (a power of two)
+
+struct NoAllocLayout {
+    size_t ctr, keys, slot_id, tkey, tkey2, pkey, tval, tval2, cnt, final_of, up_f, lo_f, hist, tmask, total;
+};
+
+constexpr size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+constexpr NoAllocLayout noalloc_layout() {
+    NoAllocLayout l{};
+    size_t o = 0;
+    l.ctr = o; o = up256(o + 8 * sizeof(uint32_t));
+    l.keys = o; o = up256(o + kNoAllocCap * sizeof(uint64_t));
+    l.slot_id = o; o = up256(o + kNoAllocCap * sizeof(uint32_t));
+    l.tkey = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint64_t));
+    l.tkey2 = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint64_t));
+    l.pkey = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint64_t));
+    l.tval = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.tval2 = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.cnt = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.final_of = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.up_f = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.lo_f = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));
+    l.hist = o; o = up256(o + kNoAllocMaxVoxels * sizeof(uint32_t));  // 256 digits x kNoAllocMaxVoxels/256 tiles
+    l.tmask = o; o = up256(o + 8 * kNoAllocMaxVoxels * sizeof(uint64_t));
+    l.total = o;
+    return l;
+}
+
+constexpr NoAllocLayout kNoAlloc = noalloc_layout();
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAlloc.total];
+
+// Device address of the static scratch array, looked up once per device with
+// that device current.
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+cudaError_t noalloc_scratch(int device, unsigned char** out) {
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_noalloc_ptr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[device] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_ptr[device]);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* arena,
+                         uint64_t arena_bytes, uint64_t* arena_needed, void* stream_v, vbm_grid* g, std::string& err) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+#define VBM_CK(call)                                                                                  \
+    do {                                                                                              \
+        const cudaError_t e_ = (call);                                                                \
+        if (e_ != cudaSuccess) {                                                                      \
+            cudaGetLastError();                                                                       \
+            err = std::string("vbm_build_device_noalloc: ") + #call + ": " + cudaGetErrorString(e_);  \
+            return VBM_ERR_CUDA;                                                                      \
+        }                                                                                             \
+    } while (0)
+    if (arena_needed) *arena_needed = 0;
+    if (n > kNoAllocMaxVoxels) {
+        err = "vbm_build_device_noalloc: " + std::to_string(n) + " voxels exceed the maximum of " +
+              std::to_string(kNoAllocMaxVoxels) + " that its static scratch memory holds";
+        return VBM_ERR_RANGE;
+    }
+    if (((uintptr_t)arena & 255u) != 0) {
+        err = "vbm_build_device_noalloc: arena must be 256-byte aligned";
+        return VBM_ERR_ALIGN;
+    }
+    int device = 0, sm = 1;
+    VBM_CK(cudaGetDevice(&device));
+    VBM_CK(cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device));
+    unsigned char* base_s = nullptr;
+    VBM_CK(noalloc_scratch(device, &base_s));
+    const uint32_t W = 1u << log2w, words = W >> 6;
+    uint32_t* ctr = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.ctr);
+    uint64_t* keys = reinterpret_cast<uint64_t*>(base_s + kNoAlloc.keys);
+    uint32_t* slot_id = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.slot_id);
+    uint64_t* tkey = reinterpret_cast<uint64_t*>(base_s + kNoAlloc.tkey);
+    uint64_t* tkey2 = reinterpret_cast<uint64_t*>(base_s + kNoAlloc.tkey2);
+    uint64_t* pkey = reinterpret_cast<uint64_t*>(base_s + kNoAlloc.pkey);
+    uint32_t* tval = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.tval);
+    uint32_t* tval2 = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.tval2);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.cnt);
+    uint32_t* final_of = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.final_of);
+    uint32_t* up_f = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.up_f);
+    uint32_t* lo_f = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.lo_f);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(base_s + kNoAlloc.hist);
+    unsigned long long* tmask = reinterpret_cast<unsigned long long*>(base_s + kNoAlloc.tmask);
+
+    // The array keeps the previous call's contents: clear what must start empty.
+    uint64_t cap = 1024;
+    while (cap < 2 * n) cap <<= 1;
+    VBM_CK(cudaMemsetAsync(ctr, 0, 8 * sizeof(uint32_t), st));
+    VBM_CK(cudaMemsetAsync(keys, 0xFF, cap * sizeof(uint64_t), st));
+    if (n) insert_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, ctr);
+    count_occupied_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, ctr + 1);
+    VBM_CK(cudaGetLastError());
+    uint32_t h[2];
+    VBM_CK(read_back(h, ctr, 2, st));
+    if (h[0] & 1u) {
+        err = "vbm_build_device_noalloc: a coordinate is outside (-2^20, 2^20)";
+        return VBM_ERR_RANGE;
+    }
+    if (h[0] & 2u) {
+        err = "vbm_build_device_noalloc: hash table overflow";
+        return VBM_ERR_CUDA;
+    }
+    const uint32_t nl = h[1];
+    VBM_CK(cudaMemsetAsync(ctr + 1, 0, sizeof(uint32_t), st));
+    VBM_CK(cudaMemsetAsync(tmask, 0, (size_t)nl * 8u * sizeof(uint64_t), st));
+    compact_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, slot_id, ctr + 1, tkey, tval, pkey);
+    if (n) mask_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, slot_id, tmask, ctr + 2);
+    VBM_CK(cudaGetLastError());
+    uint32_t dups = 0;
+    VBM_CK(read_back(&dups, ctr + 2, 1, st));
+    if (dups && !(flags & VBM_BUILD_DEDUP)) {
+        err = "vbm_build_device_noalloc: duplicate coordinates (" + std::to_string(dups) + " repeats)";
+        return VBM_ERR_DUPLICATE;
+    }
+    if (nl) {
+        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, nl, 54, st));
+        count_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, final_of);
+        node_flag_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(cnt, nl, ctr + 5);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(up_f, nl, ctr + 6);
+        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(lo_f, nl, ctr + 7);
+        VBM_CK(cudaGetLastError());
+    }
+    uint32_t tot[3] = {0, 0, 0};
+    if (nl) VBM_CK(read_back(tot, ctr + 5, 3, st));
+    const uint64_t N = tot[0];
+    const uint64_t n_blocks = (N + W - 1) / W;
+    const ArenaLayout lay = arena_layout(nl, tot[1], tot[2], n_blocks, log2w);
+    if (arena_needed) *arena_needed = lay.total;
+    if (!arena || arena_bytes < lay.total) {
+        err = "vbm_build_device_noalloc: the arena holds " + std::to_string(arena_bytes) + " bytes; this grid needs " +
+              std::to_string(lay.total);
+        return VBM_ERR_RANGE;
+    }
+    g->n = N;
+    g->log2w = log2w;
+    g->n_leaves = nl;
+    g->n_upper = tot[1];
+    g->n_lower = tot[2];
+    g->n_blocks = n_blocks;
+    g->device = device;
+    g->arena = arena;
+    g->arena_bytes = lay.total;
+    g->owns_arena = false;
+    g->host_mirrors = false;
+    char* base = static_cast<char*>(arena);
+    LeafRec* leaves = reinterpret_cast<LeafRec*>(base + lay.off[0]);
+    uint64_t* root_keys = reinterpret_cast<uint64_t*>(base + lay.off[1]);
+    uint32_t* upper = reinterpret_cast<uint32_t*>(base + lay.off[2]);
+    uint32_t* lower = reinterpret_cast<uint32_t*>(base + lay.off[3]);
+    uint32_t* first_leaf = reinterpret_cast<uint32_t*>(base + lay.off[4]);
+    unsigned long long* jump = reinterpret_cast<unsigned long long*>(base + lay.off[5]);
+    uint32_t* nbr = reinterpret_cast<uint32_t*>(base + lay.off[6]);
+    VBM_CK(cudaMemsetAsync(upper, 0xFF, lay.bytes[2], st));
+    VBM_CK(cudaMemsetAsync(lower, 0xFF, lay.bytes[3], st));
+    VBM_CK(cudaMemsetAsync(jump, 0, lay.bytes[5], st));
+    VBM_CK(cudaMemsetAsync(ctr + 3, 0, 2 * sizeof(uint32_t), st));
+    if (nl) {
+        leafrec_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, pkey, leaves);
+        tables_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f, leaves, root_keys, upper, lower);
+        blocks_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(leaves, nl, log2w, first_leaf, jump);
+        nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
+                                                                                 final_of, nbr);
+        span_kernel<<<grid_for(n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)n_blocks, words, ctr + 3);
+        VBM_CK(cudaGetLastError());
+    }
+    uint32_t spans[2] = {0, 0};
+    VBM_CK(read_back(spans, ctr + 3, 2, st));
+    g->max_span = spans[0];
+    g->n_over_cache = spans[1];
+    set_device_views(g, lay, sm);
+#undef VBM_CK
+    return VBM_OK;
+}
+
 }  // namespace vbm

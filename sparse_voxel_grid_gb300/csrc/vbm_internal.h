@@ -90,6 +90,8 @@ struct vbm_grid {
     // device arena (one allocation) and the views into it
     void* arena = nullptr;
     size_t arena_bytes = 0;
+    bool owns_arena = true;    // false: the arena is the caller's (vbm_build_device_noalloc)
+    bool host_mirrors = true;  // false: no host copies of the arrays (vbm_build_device_noalloc)
     int device = -1;
     vbm::DevGrid dev{};
 };
@@ -150,4 +152,9 @@ int build_host(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, vbm
 // Fills the device arena and the host mirrors of g; synchronises `stream`.
 int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* stream, vbm_grid* g,
                  std::string& err);
+
+// Allocation-free device builder (vbm_build_device_noalloc): temporary memory
+// in a static device array, the grid's arrays in the caller's `arena`.
+int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* arena,
+                         uint64_t arena_bytes, uint64_t* arena_needed, void* stream, vbm_grid* g, std::string& err);
 }  // namespace vbm
