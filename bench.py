@@ -109,6 +109,18 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` over the ranks of the default process group (any
+    backend); `value` itself when no group is initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -182,9 +194,7 @@ def run_gpu(args):
     step_ms = [sum(per_c_ms[C][k] for C in CS) for k in range(args.steps)]
     ms_per_step = statistics.mean(step_ms)
     if dist:
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+        ms_per_step = max_over_ranks(ms_per_step, device="cuda")
     value = world * len(CS) * n / (ms_per_step * 1e-3)
 
     peak_gbs, peak_kind = peaks()
