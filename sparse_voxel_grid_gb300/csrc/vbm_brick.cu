@@ -99,7 +99,7 @@ __host__ __device__ constexpr size_t brick_smem_bytes(int log2w) {
 // Decode every valid slot of the block (select-based decode, [2258] "What
 // changed") into offs/lof and record where each spanned leaf starts.  Ends with
 // a barrier.
-__device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
+__device__ __forceinline__ void brick_prologue_direct(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
                                                uint16_t* starts) {
     k.W = 1u << g.log2w;
     const uint32_t words = k.W >> 6;
@@ -116,6 +116,59 @@ __device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, ui
     }
     if (threadIdx.x == 0) starts[k.span] = (uint16_t)k.n_valid;
     __syncthreads();
+}
+
+__device__ __forceinline__ void brick_prologue_staged(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
+                                               uint16_t* starts) {
+    // The block's jumpMap words and their popcount prefixes, staged once.
+    __shared__ uint64_t s_jw[8];
+    __shared__ uint32_t s_cum[9];
+    k.W = 1u << g.log2w;
+    const uint32_t words = k.W >> 6;
+    k.b = blockIdx.x;
+    k.jb = g.jump + (size_t)k.b * words;
+    k.fl = __ldg(&g.first_leaf[k.b]);
+    k.n_valid = min(k.W, g.n - k.b * k.W);
+    if (threadIdx.x < 32u) {
+        const uint32_t lane = threadIdx.x;
+        const uint64_t w = lane < words ? __ldg(&k.jb[lane]) : 0ull;
+        const uint32_t c = (uint32_t)__popcll(w);
+        uint32_t incl = c;
+#pragma unroll
+        for (int d = 1; d < 8; d <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= (uint32_t)d) incl += t;
+        }
+        if (lane < words) {
+            s_jw[lane] = w;
+            s_cum[lane] = incl - c;
+        }
+        if (lane == words - 1u) s_cum[words] = incl;
+    }
+    __syncthreads();
+    k.span = 1u + s_cum[words];
+    for (uint32_t s = threadIdx.x; s < k.n_valid; s += blockDim.x) {
+        const uint32_t ws = s >> 6;
+        const uint64_t jw = s_jw[ws];
+        const uint32_t leaf = k.fl + s_cum[ws] + (uint32_t)__popcll(jw & ((2ull << (s & 63u)) - 1ull));
+        const LeafRec* rec = g.leaves + leaf;
+        const uint32_t off = leaf_select(rec, 1u + k.b * k.W + s - __ldg(&rec->first));
+        offs[s] = (uint16_t)off;
+        lof[s] = (uint16_t)(leaf - k.fl);
+        if (s == 0 || ((jw >> (s & 63u)) & 1ull)) starts[leaf - k.fl] = (uint16_t)s;
+    }
+    if (threadIdx.x == 0) starts[k.span] = (uint16_t)k.n_valid;
+    __syncthreads();
+}
+
+// STAGED: jumpMap words and popcount prefixes in shared memory (faster for
+// the one-lane layouts); otherwise each thread ranks from global memory
+// (measured faster for the float4-lane layouts).
+template <bool STAGED>
+__device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
+                                               uint16_t* starts) {
+    if constexpr (STAGED) brick_prologue_staged(g, k, offs, lof, starts);
+    else brick_prologue_direct(g, k, offs, lof, starts);
 }
 
 // Build the bricks of spanned leaves l0 .. l0+nb-1 into ib[0..nb).  Leaf l's
@@ -253,7 +306,7 @@ __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const floa
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
-    brick_prologue(g, k, m.offs, m.lof, m.starts);
+    brick_prologue<!VEC>(g, k, m.offs, m.lof, m.starts);
     const uint32_t L = CT > 0 ? (uint32_t)(CT / CC) : (uint32_t)lanes;
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
@@ -284,7 +337,7 @@ __global__ void __launch_bounds__(512) brick_taps_kernel(DevGrid g, uint32_t* __
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
-    brick_prologue(g, k, m.offs, m.lof, m.starts);
+    brick_prologue<true>(g, k, m.offs, m.lof, m.starts);
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
