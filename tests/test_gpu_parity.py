@@ -141,3 +141,22 @@ def test_device_errors():
     assert lib.vbm_box_filter(g.handle, ok, 1, mis, 7, 0, None) == -1
     assert lib.vbm_cross_filter(g.handle, ok, 1, ok2, 1, 5, None) == -1
     assert b"op" in lib.vbm_last_error()
+
+
+def test_host_pipeline_matches_direct_calls():
+    """HostPipeline (overlapped host<->device copies) returns the same bits as
+    vbm_box_filter on device tensors, on two runs in a row."""
+    t = gu.torch()
+    coords = SMALL["tiny_shell"]()
+    o = oracle.OracleGrid(coords)
+    g = vbm.vbm_build(coords, 7)
+    widths = (1, 3, 8)
+    pipe = vbm.HostPipeline(g, widths)
+    for run in range(2):
+        host_in = {C: t.from_numpy(synth.sidecar_uniform(o.n, C, seed=run * 10 + C)).pin_memory() for C in widths}
+        host_out = {C: t.empty_like(host_in[C]).pin_memory() for C in widths}
+        pipe.run(host_in, host_out)
+        pipe.synchronize()
+        for C in widths:
+            want = o.box_filter(host_in[C].numpy(), C)
+            np.testing.assert_array_equal(gu.bits(host_out[C].numpy()), gu.bits(want))
