@@ -342,8 +342,9 @@ def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
             res.append({"kernel": "laplacian", "W": 1 << log2w, "C": 1, "resolver": rname, "ms": round(ms, 5)})
         li = torch.empty(g.n_slots, dtype=torch.int32, device="cuda")
         vo = torch.empty(g.n_slots, dtype=torch.int16, device="cuda")
-        ms = tmean(lambda: vbm.vbm_decode(g, li, vo))
-        res.append({"kernel": "decode", "W": 1 << log2w, "ms": round(ms, 5)})
+        for mname, fn in (("select", vbm.vbm_decode), ("sweep", vbm.vbm_decode_sweep)):
+            ms = tmean(lambda: fn(g, li, vo))
+            res.append({"kernel": "decode", "method": mname, "W": 1 << log2w, "ms": round(ms, 5)})
         g.close()
     return res
 
@@ -416,6 +417,57 @@ def run_reference(args):
     }))
 
 
+def run_decode_ab(args):
+    """Select decode against the sweep decode it replaced, on the shells and
+    the decode grid D at every block width: median of --steps cold-cache
+    launches each (L2 flushed before every launch), outputs compared byte for
+    byte.  Prints one JSON line."""
+    import torch
+    import sparse_voxel_grid_gb300 as vbm
+    import synth
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device="cuda")
+
+    def median_us(fn):
+        for _ in range(args.warmup):
+            fn()
+        evs = []
+        for _ in range(args.steps):
+            flush_buf.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+    rows = []
+    for name in ("S185", "S160", "D"):
+        coords = torch.from_numpy(synth.WORKLOADS[name]()).cuda()
+        for log2w in (6, 7, 8, 9):
+            g = vbm.vbm_build_device(coords, log2w)
+            m = g.n_slots
+            maps = {}
+            for mname, fn in (("select", vbm.vbm_decode), ("sweep", vbm.vbm_decode_sweep)):
+                li = torch.full((m,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+                vo = torch.full((m,), 0x5555, dtype=torch.int16, device="cuda")
+                maps[mname] = (li, vo, median_us(lambda: fn(g, li, vo)))
+            same = bool(torch.equal(maps["select"][0], maps["sweep"][0]) and
+                        torch.equal(maps["select"][1], maps["sweep"][1]))
+            sel, swp = maps["select"][2], maps["sweep"][2]
+            rows.append({"workload": name, "n": g.n, "leaves": g.info["n_leaves"], "W": 1 << log2w,
+                         "select_us": round(sel, 2), "sweep_us": round(swp, 2), "speedup": round(swp / sel, 3),
+                         "identical": same})
+            g.close()
+        del coords
+    print(json.dumps({"metric": "decode: select vs sweep", "unit": "us (median, L2 flushed)", "steps": args.steps,
+                      "warmup": args.warmup, "rows": rows}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,10 +482,14 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-ab", action="store_true",
+                    help="time the select decode against the sweep decode and print that table instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.decode_ab:
+        run_decode_ab(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -186,6 +186,14 @@ int vbm_leaf_export(const vbm_grid* grid, int what, void* dst, uint64_t bytes);
  * Errors: INVALID, STATE, ALIGN, CUDA. */
 int vbm_decode(const vbm_grid* grid, uint32_t* leaf_index, uint16_t* voxel_offset, void* stream);
 
+/* Sweep decode, the design the select decode replaced ([2258] "What changed";
+ * timed against it in [2258] "A/B — decode"): one CTA per block, whose threads
+ * sweep all 512 voxel slots of every leaf overlapping the block and keep the
+ * active voxels whose index lies in the block; O(span x 512) work per block.
+ * Same arguments, outputs (bit for bit) and errors as vbm_decode.  Provided
+ * to reproduce the select-versus-sweep comparison. */
+int vbm_decode_sweep(const vbm_grid* grid, uint32_t* leaf_index, uint16_t* voxel_offset, void* stream);
+
 /* 27-tap box filter ([2262] "What changed", "A/B"; [2263] "Measurements"): for
  * every active voxel v and channel ch,
  *     out[v*C+ch] = sum over taps t = (di+1)*9+(dj+1)*3+(dk+1), t = 0..26, of

@@ -44,7 +44,7 @@ SENTINEL_OFFSET = 0xFFFF
 
 __all__ = [
     "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
-    "vbm_box_filter", "vbm_cross_filter", "vbm_box_taps", "vbm_cross_taps", "vbm_last_error",
+    "vbm_decode_sweep", "vbm_box_filter", "vbm_cross_filter", "vbm_box_taps", "vbm_cross_taps", "vbm_last_error",
 ]
 
 
@@ -171,6 +171,15 @@ def vbm_decode(grid: Grid, leaf_index, voxel_offset, stream=None) -> None:
     m = grid.n_slots
     check(load().vbm_decode(grid.handle, _dev_ptr(leaf_index, torch.int32, m, "leaf_index"),
                             _dev_ptr(voxel_offset, torch.int16, m, "voxel_offset"), _stream_handle(stream)))
+
+
+def vbm_decode_sweep(grid: Grid, leaf_index, voxel_offset, stream=None) -> None:
+    """The sweep decode (the select decode's predecessor): same arguments and
+    the same output bits as vbm_decode."""
+    import torch
+    m = grid.n_slots
+    check(load().vbm_decode_sweep(grid.handle, _dev_ptr(leaf_index, torch.int32, m, "leaf_index"),
+                                  _dev_ptr(voxel_offset, torch.int16, m, "voxel_offset"), _stream_handle(stream)))
 
 
 def vbm_box_filter(grid: Grid, sidecar, C: int, out, resolver: int = RESOLVE_CACHED,

@@ -81,6 +81,8 @@ def load(path: str = LIB_PATH):
             lib.vbm_leaf_export.argtypes = [p, i32, p, u64]
             lib.vbm_decode.restype = i32
             lib.vbm_decode.argtypes = [p, p, p, p]
+            lib.vbm_decode_sweep.restype = i32
+            lib.vbm_decode_sweep.argtypes = [p, p, p, p]
             lib.vbm_box_filter.restype = i32
             lib.vbm_box_filter.argtypes = [p, p, i32, p, i32, i32, p]
             lib.vbm_cross_filter.restype = i32

@@ -259,6 +259,19 @@ int vbm_decode(const vbm_grid* g, uint32_t* leaf_index, uint16_t* voxel_offset, 
     return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_decode: launch", e);
 }
 
+int vbm_decode_sweep(const vbm_grid* g, uint32_t* leaf_index, uint16_t* voxel_offset, void* stream) {
+    g_last_error.clear();
+    int rc = check_grid(g, "vbm_decode_sweep");
+    if (rc) return rc;
+    if (g->n_blocks == 0) return VBM_OK;
+    if ((rc = check_ptr(leaf_index, "vbm_decode_sweep", "leaf_index"))) return rc;
+    if ((rc = check_ptr(voxel_offset, "vbm_decode_sweep", "voxel_offset"))) return rc;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_decode_sweep: cannot select the grid's device");
+    cudaError_t e = vbm::launch_sweep_decode(g->dev, leaf_index, voxel_offset, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_decode_sweep: launch", e);
+}
+
 static int check_filter(const vbm_grid* g, const float* sidecar, int C, const float* out, int resolver,
                         const char* fn) {
     int rc = check_grid(g, fn);

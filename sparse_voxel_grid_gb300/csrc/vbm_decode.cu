@@ -110,6 +110,36 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
     }
 }
 
+// Sweep decode: the design the select decode replaced (OpenVDB PR #2258,
+// "What changed"), kept as its A/B baseline.  One CTA of W threads per block;
+// the threads jointly sweep all 512 voxel slots of every leaf overlapping the
+// block (the leaf holding the block's first index and the `popcount(jumpMap)`
+// leaves that start inside it), compute each active voxel's index and keep the
+// ones that fall inside the block: O(span x 512) work per block, with a
+// data-dependent branch per voxel.  Output identical to the select decode.
+__global__ void __launch_bounds__(512) sweep_decode_kernel(DevGrid g, uint32_t* __restrict__ leaf_index,
+                                                           uint16_t* __restrict__ voxel_offset) {
+    const uint32_t log2w = (uint32_t)g.log2w, W = 1u << log2w, words = W >> 6;
+    const uint32_t b = blockIdx.x, tid = threadIdx.x;
+    const uint32_t first = 1u + (b << log2w);  // index of the block's slot 0
+    const uint32_t slot = (b << log2w) + tid;
+    if (slot >= g.n) {  // index = slot + 1 > N
+        leaf_index[slot] = kNone;
+        voxel_offset[slot] = kNoOffset;
+    }
+    const uint32_t fl = __ldg(&g.first_leaf[b]);
+    const uint32_t span = block_span(g.jump + (size_t)b * words, words);
+    for (uint32_t l = 0; l < span; ++l) {
+        for (uint32_t off = tid; off < 512u; off += W) {
+            const uint32_t idx = leaf_index_at(g.leaves, fl + l, off);
+            if (idx != 0 && idx - first < W) {
+                leaf_index[idx - 1u] = fl + l;
+                voxel_offset[idx - 1u] = (uint16_t)off;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream) {
@@ -126,6 +156,12 @@ cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxe
     const uint64_t max_cta = (n_slots + 63) / 64;  // at least 64 slots per CTA
     if (n_cta > max_cta) n_cta = max_cta;
     decode_kernel<<<(unsigned)n_cta, kDecodeThreads, 0, stream>>>(g, (uint32_t)n_cta, leaf_index, voxel_offset);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sweep_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream) {
+    if (g.n_blocks == 0) return cudaSuccess;
+    sweep_decode_kernel<<<(unsigned)g.n_blocks, threads_for(g.log2w), 0, stream>>>(g, leaf_index, voxel_offset);
     return cudaGetLastError();
 }
 

@@ -9,6 +9,7 @@
 namespace vbm {
 
 cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream);
+cudaError_t launch_sweep_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxel_offset, cudaStream_t stream);
 
 cudaError_t launch_box_filter(const DevGrid& g, const float* sidecar, int C, float* out, int resolver, int output,
                               cudaStream_t stream);

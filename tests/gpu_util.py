@@ -25,12 +25,14 @@ def to_dev(a: np.ndarray):
     return t.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def decode(g):
+def decode(g, method="select"):
+    """Decode maps as (uint32, uint16) host arrays.  The buffers start filled
+    with values no decode writes, so a slot left unwritten shows up."""
     t = torch()
     m = g.n_slots
-    li = t.empty(m, dtype=t.int32, device="cuda")
-    vo = t.empty(m, dtype=t.int16, device="cuda")
-    vbm.vbm_decode(g, li, vo)
+    li = t.full((m,), 0x5A5A5A5A, dtype=t.int32, device="cuda")
+    vo = t.full((m,), 0x5555, dtype=t.int16, device="cuda")
+    {"select": vbm.vbm_decode, "sweep": vbm.vbm_decode_sweep}[method](g, li, vo)
     t.cuda.synchronize()
     return li.cpu().numpy().view(np.uint32), vo.cpu().numpy().view(np.uint16)
 

@@ -50,11 +50,12 @@ def case(request):
     return request.param, coords, oracle.OracleGrid(coords)
 
 
+@pytest.mark.parametrize("method", ["select", "sweep"])
 @pytest.mark.parametrize("log2w", [6, 7, 8, 9])
-def test_decode(case, log2w):
+def test_decode(case, log2w, method):
     _, coords, o = case
     g = vbm.vbm_build(coords, log2w)
-    li, vo = gu.decode(g)
+    li, vo = gu.decode(g, method)
     wli, wvo = o.decode(log2w)
     np.testing.assert_array_equal(li, wli)
     np.testing.assert_array_equal(vo, wvo)
@@ -118,6 +119,9 @@ def test_empty_grid():
     vbm.vbm_cross_filter(g, s, 3, out)
     taps = t.full((27,), 9, dtype=t.int32, device="cuda")
     vbm.vbm_box_taps(g, taps)
+    lib = vbm.load()
+    assert lib.vbm_decode(g.handle, None, None, None) == 0  # no slots: nothing to write
+    assert lib.vbm_decode_sweep(g.handle, None, None, None) == 0
     t.cuda.synchronize()
     assert (out.cpu() == 0).all() and (taps.cpu() == 0).all()
 
@@ -141,6 +145,10 @@ def test_device_errors():
     assert lib.vbm_box_filter(g.handle, ok, 1, mis, 7, 0, None) == -1
     assert lib.vbm_cross_filter(g.handle, ok, 1, ok2, 1, 5, None) == -1
     assert b"op" in lib.vbm_last_error()
+    for fn in (lib.vbm_decode, lib.vbm_decode_sweep):
+        assert fn(g.handle, None, ok, None) == -1
+        assert fn(g.handle, mis, ok, None) == -6
+        assert fn(g.handle, ok, mis, None) == -6
 
 
 def test_host_pipeline_matches_direct_calls():

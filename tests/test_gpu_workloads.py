@@ -38,11 +38,12 @@ def shell():
     return coords, oracle.OracleGrid(coords)
 
 
+@pytest.mark.parametrize("method", ["select", "sweep"])
 @pytest.mark.parametrize("log2w", [6, 7, 8, 9])
-def test_shell_decode_full(shell, log2w):
+def test_shell_decode_full(shell, log2w, method):
     coords, o = shell
     g = vbm.vbm_build(coords, log2w)
-    li, vo = gu.decode(g)
+    li, vo = gu.decode(g, method)
     wli, wvo = o.decode(log2w)
     np.testing.assert_array_equal(li, wli)
     np.testing.assert_array_equal(vo, wvo)
@@ -99,11 +100,12 @@ def bricks():
     return coords, oracle.OracleGrid(coords)
 
 
+@pytest.mark.parametrize("method", ["select", "sweep"])
 @pytest.mark.parametrize("log2w", [6, 7, 8, 9])
-def test_decode_grid_full(bricks, log2w):
+def test_decode_grid_full(bricks, log2w, method):
     coords, o = bricks
     g = vbm.vbm_build(coords, log2w)
-    li, vo = gu.decode(g)
+    li, vo = gu.decode(g, method)
     wli, wvo = o.decode(log2w)
     np.testing.assert_array_equal(li, wli)
     np.testing.assert_array_equal(vo, wvo)
