@@ -65,6 +65,8 @@ def _load():
             lib.oracle_box_filter.argtypes = [p, p, i32, p, i64, p]
             lib.oracle_cross_filter.restype = i32
             lib.oracle_cross_filter.argtypes = [p, p, i32, i32, p, i64, p]
+            lib.oracle_weno_filter.restype = None
+            lib.oracle_weno_filter.argtypes = [p, p, ctypes.c_float, p, i64, p]
             _lib = lib
     return _lib
 
@@ -143,7 +145,7 @@ class OracleGrid:
         out = np.empty((rows, shape), dtype=np.uint32)
         rc = self._lib.oracle_taps(self._h, shape, _ptr(w), m, _ptr(out))
         if rc:
-            raise ValueError("oracle: shape must be 27 or 7")
+            raise ValueError("oracle: shape must be 27, 19 or 7")
         return out
 
     def box_filter(self, sidecar: np.ndarray, C: int, which=None) -> np.ndarray:
@@ -164,4 +166,15 @@ class OracleGrid:
         rc = self._lib.oracle_cross_filter(self._h, _ptr(s), C, op, _ptr(w), m, _ptr(out))
         if rc:
             raise ValueError("oracle: op must be 0 (Laplacian) or 1 (7-tap sum)")
+        return out
+
+    def weno_filter(self, phi: np.ndarray, iso: float = 0.0, which=None) -> np.ndarray:
+        """19-tap WENO consumer: Godunov squared gradient norm of phi (N+1
+        float32 rows, row 0 the background) at each row."""
+        s = np.ascontiguousarray(phi, dtype=np.float32)
+        assert s.size == self.n + 1
+        w, m = self._which(which)
+        rows = m if w is not None else self.n + 1
+        out = np.empty(rows, dtype=np.float32)
+        self._lib.oracle_weno_filter(self._h, _ptr(s), float(iso), _ptr(w), m, _ptr(out))
         return out

@@ -33,6 +33,15 @@
  *   - Laplacian (the 7-point consumer [2258] "A/B - decode" names): s = +0;
  *     s += face value for each active face in increasing t; out = s - 6*centre
  *     with the product and the difference rounded separately.
+ *   - 19-tap WENO consumer ([2258] "A/B - decode" names it, no formula): the
+ *     taps are the centre and the voxels 1, 2, 3 steps away along each axis, in
+ *     increasing (di,dj,dk) lexicographic order (the box order restricted, as
+ *     for the cross).  An inactive tap reads sidecar row 0, the background
+ *     value's slot of an index grid.  The value is the Godunov upwind squared
+ *     gradient norm of a level set phi at unit spacing, built from fifth-order
+ *     WENO one-sided derivatives (Jiang & Shu, J. Comput. Phys. 126, 1996;
+ *     Jiang & Peng, SIAM J. Sci. Comput. 21, 2000) with epsilon = 1e-6, all in
+ *     fp32 with each operation rounded, in the order written below.
  * Build: g++ -std=c++20 -O2 -ffp-contract=off (no FMA, no fast-math).
  */
 #include <algorithm>
@@ -83,6 +92,63 @@ void tap_offset(int t, int& di, int& dj, int& dk) {
 }
 
 const int kCrossTaps[7] = {4, 10, 12, 13, 14, 16, 22};
+
+// 19-tap WENO stencil: offsets in increasing (di,dj,dk) lexicographic order.
+const int kWenoOffsets[19][3] = {{-3, 0, 0}, {-2, 0, 0}, {-1, 0, 0}, {0, -3, 0}, {0, -2, 0}, {0, -1, 0}, {0, 0, -3},
+                                 {0, 0, -2}, {0, 0, -1}, {0, 0, 0},  {0, 0, 1},  {0, 0, 2},  {0, 0, 3},  {0, 1, 0},
+                                 {0, 2, 0},  {0, 3, 0},  {1, 0, 0},  {2, 0, 0},  {3, 0, 0}};
+
+// Fifth-order WENO approximation of a one-sided derivative from five
+// consecutive first differences a..e (upwind side first).  Three third-order
+// candidates on the sub-stencils (a,b,c), (b,c,d), (c,d,e); smoothness
+// indicators s_k; weights alpha_k = gamma_k / (s_k + eps)^2 with the ideal
+// weights gamma = 0.1, 0.6, 0.3; result = sum alpha_k q_k / (6 sum alpha_k),
+// where q_k is six times the k-th candidate.
+float weno5(float a, float b, float c, float d, float e) {
+    const float k13_12 = 13.0f / 12.0f;
+    const float eps = 1.0e-6f;
+    const float t1 = a - 2.0f * b + c;
+    const float t2 = a - 4.0f * b + 3.0f * c;
+    const float s1 = k13_12 * (t1 * t1) + 0.25f * (t2 * t2);
+    const float u1 = b - 2.0f * c + d;
+    const float u2 = b - d;
+    const float s2 = k13_12 * (u1 * u1) + 0.25f * (u2 * u2);
+    const float v1 = c - 2.0f * d + e;
+    const float v2 = 3.0f * c - 4.0f * d + e;
+    const float s3 = k13_12 * (v1 * v1) + 0.25f * (v2 * v2);
+    const float r1 = s1 + eps, r2 = s2 + eps, r3 = s3 + eps;
+    const float w1 = 0.1f / (r1 * r1);
+    const float w2 = 0.6f / (r2 * r2);
+    const float w3 = 0.3f / (r3 * r3);
+    const float q1 = 2.0f * a - 7.0f * b + 11.0f * c;
+    const float q2 = -b + 5.0f * c + 2.0f * d;
+    const float q3 = 2.0f * c + 5.0f * d - e;
+    const float num = w1 * q1 + w2 * q2 + w3 * q3;
+    const float den = 6.0f * (w1 + w2 + w3);
+    return num / den;
+}
+
+// Godunov upwind square of the derivative along one axis from the values
+// p[0..6] at offsets -3..+3 (p[3] the centre).  minus / plus: the left- and
+// right-biased WENO derivatives.  Outside the level set (centre > iso) the
+// positive part of minus and the negative part of plus compete, inside the
+// opposite parts; the larger square wins.
+float godunov_axis(const float (&p)[7], bool outside) {
+    float d[6];  // d[k] = p[k+1] - p[k]: differences at offsets -2..+3
+    for (int k = 0; k < 6; ++k) d[k] = p[k + 1] - p[k];
+    const float minus = weno5(d[0], d[1], d[2], d[3], d[4]);
+    const float plus = weno5(d[5], d[4], d[3], d[2], d[1]);
+    float lo, hi;
+    if (outside) {
+        lo = minus > 0.0f ? minus : 0.0f;
+        hi = plus < 0.0f ? plus : 0.0f;
+    } else {
+        lo = minus < 0.0f ? minus : 0.0f;
+        hi = plus > 0.0f ? plus : 0.0f;
+    }
+    const float lo2 = lo * lo, hi2 = hi * hi;
+    return lo2 > hi2 ? lo2 : hi2;
+}
 
 }  // namespace
 
@@ -212,10 +278,11 @@ void oracle_blocks(const oracle_grid* g, int log2w, uint32_t* first_leaf, uint64
 
 // Stencil taps of the voxels with indices which[0..m) (all 1..N when which is
 // NULL, rows 0..N with row 0 zero).  shape 27: the box, taps in order
-// t = (di+1)*9+(dj+1)*3+(dk+1); shape 7: the cross, taps {4,10,12,13,14,16,22}.
+// t = (di+1)*9+(dj+1)*3+(dk+1); shape 7: the cross, taps {4,10,12,13,14,16,22};
+// shape 19: the WENO stencil (kWenoOffsets).
 // taps[r*shape + j] = index of the neighbour, 0 if inactive.
 int oracle_taps(const oracle_grid* g, int shape, const int64_t* which, int64_t m, uint32_t* taps) {
-    if (shape != 27 && shape != 7) return -1;
+    if (shape != 27 && shape != 7 && shape != 19) return -1;
     int64_t n = (int64_t)g->vox.size();
     int64_t rows = which ? m : n + 1;
     for (int64_t r = 0; r < rows; ++r) {
@@ -225,7 +292,13 @@ int oracle_taps(const oracle_grid* g, int shape, const int64_t* which, int64_t m
             if (index >= 1 && index <= n) {
                 const Voxel& c = g->vox[(size_t)index - 1];
                 int di, dj, dk;
-                tap_offset(shape == 27 ? j : kCrossTaps[j], di, dj, dk);
+                if (shape == 19) {
+                    di = kWenoOffsets[j][0];
+                    dj = kWenoOffsets[j][1];
+                    dk = kWenoOffsets[j][2];
+                } else {
+                    tap_offset(shape == 27 ? j : kCrossTaps[j], di, dj, dk);
+                }
                 v = (uint32_t)oracle_index(g, c.x + di, c.y + dj, c.z + dk);
             }
             taps[r * shape + j] = v;
@@ -291,6 +364,35 @@ int oracle_cross_filter(const oracle_grid* g, const float* sidecar, int C, int o
         }
     }
     return 0;
+}
+
+// 19-tap WENO consumer: out[r] = the Godunov squared gradient norm of phi at
+// the voxel (sum over x, y, z of godunov_axis, added in that order); phi has
+// N+1 rows, row 0 the background value that inactive taps read.  Rows as in
+// oracle_taps; row 0 and rows outside 1..N are +0.
+void oracle_weno_filter(const oracle_grid* g, const float* phi, float iso, const int64_t* which, int64_t m,
+                        float* out) {
+    int64_t n = (int64_t)g->vox.size();
+    int64_t rows = which ? m : n + 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t index = which ? which[r] : r;
+        out[r] = 0.0f;
+        if (index < 1 || index > n) continue;
+        const Voxel& c = g->vox[(size_t)index - 1];
+        const bool outside = phi[index] > iso;
+        float total = 0.0f;
+        for (int axis = 0; axis < 3; ++axis) {
+            float p[7];
+            for (int k = -3; k <= 3; ++k) {
+                int q[3] = {0, 0, 0};
+                q[axis] = k;
+                int64_t nb = oracle_index(g, c.x + q[0], c.y + q[1], c.z + q[2]);
+                p[k + 3] = phi[nb];  // nb == 0: the background row
+            }
+            total = total + godunov_axis(p, outside);
+        }
+        out[r] = total;
+    }
 }
 
 }  // extern "C"
