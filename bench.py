@@ -340,6 +340,8 @@ def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
                          ("brick", vbm.RESOLVE_BRICK)):
             ms = tmean(lambda: vbm.vbm_cross_filter(g, sidecars[1], 1, outs[1], r, vbm.CROSS_LAPLACIAN))
             res.append({"kernel": "laplacian", "W": 1 << log2w, "C": 1, "resolver": rname, "ms": round(ms, 5)})
+            ms = tmean(lambda: vbm.vbm_weno_filter(g, sidecars[1], outs[1], 0.0, r))
+            res.append({"kernel": "weno", "W": 1 << log2w, "C": 1, "resolver": rname, "ms": round(ms, 5)})
         li = torch.empty(g.n_slots, dtype=torch.int32, device="cuda")
         vo = torch.empty(g.n_slots, dtype=torch.int16, device="cuda")
         for mname, fn in (("select", vbm.vbm_decode), ("sweep", vbm.vbm_decode_sweep)):

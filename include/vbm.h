@@ -224,6 +224,26 @@ int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out
 int vbm_cross_filter(const vbm_grid* grid, const float* sidecar, int C, float* out, int resolver, int op,
                      void* stream);
 
+/* 19-tap WENO consumer ([2258] "A/B - decode" names it beside the box and
+ * the Laplacian; the pages give no formula, so this one is a reading): for
+ * every active voxel v,
+ *     out[v] = Godunov upwind squared gradient norm of the level set phi at v,
+ * at unit spacing, from fifth-order WENO one-sided derivatives (Jiang & Shu
+ * 1996; Jiang & Peng 2000; epsilon 1e-6).  Taps j = 0..18: the centre and the
+ * voxels 1, 2, 3 steps away along each axis, in increasing (di,dj,dk)
+ * lexicographic order; an inactive tap reads phi[0], the background value.
+ * Per axis, with p[-3..3] the tap values and d[k] = p[k] - p[k-1]:
+ *     minus = WENO5(d[-2], d[-1], d[0], d[1], d[2]),
+ *     plus  = WENO5(d[3], d[2], d[1], d[0], d[-1]);
+ * outside (phi[v] > iso) the axis term is max(max(minus,0)^2, min(plus,0)^2),
+ * inside max(min(minus,0)^2, max(plus,0)^2); out[v] = x term + y term + z term
+ * in that order.  All in fp32, each operation rounded separately (no FMA), so
+ * every resolver gives the same bits.  Scale by 1/dx^2 for spacing dx.
+ * phi and out: device arrays of N+1 floats (out may not alias phi); out[0] is
+ * written as +0.0.  resolver: VBM_RESOLVE_*.  Errors: INVALID, STATE, ALIGN,
+ * CUDA. */
+int vbm_weno_filter(const vbm_grid* grid, const float* phi, float iso, float* out, int resolver, void* stream);
+
 /* Raw taps for byte-exact validation ([2263] "Validation": all taps of every
  * thread materialised to global memory): taps[v*27 + t] (box) or taps[v*7 + j]
  * (cross) is the index of that neighbour of voxel v, 0 if inactive; row 0 is
@@ -231,6 +251,11 @@ int vbm_cross_filter(const vbm_grid* grid, const float* sidecar, int C, float* o
  * Errors: INVALID, STATE, ALIGN, CUDA. */
 int vbm_box_taps(const vbm_grid* grid, uint32_t* taps, int resolver, void* stream);
 int vbm_cross_taps(const vbm_grid* grid, uint32_t* taps, int resolver, void* stream);
+
+/* Raw taps of the 19-tap WENO stencil, as vbm_box_taps: taps[v*19 + j] is the
+ * index of tap j of voxel v (order as in vbm_weno_filter), 0 if inactive; row
+ * 0 is all zeros.  taps is a device array of (N+1)*19 uint32. */
+int vbm_weno_taps(const vbm_grid* grid, uint32_t* taps, int resolver, void* stream);
 
 #ifdef __cplusplus
 }

@@ -39,12 +39,14 @@ EXPORT = {
 }
 BOX_TAPS = 27
 CROSS_TAPS = 7
+WENO_TAPS = 19
 SENTINEL_LEAF = 0xFFFFFFFF
 SENTINEL_OFFSET = 0xFFFF
 
 __all__ = [
     "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
-    "vbm_decode_sweep", "vbm_box_filter", "vbm_cross_filter", "vbm_box_taps", "vbm_cross_taps", "vbm_last_error",
+    "vbm_decode_sweep", "vbm_box_filter", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
+    "vbm_weno_taps", "vbm_last_error",
 ]
 
 
@@ -214,6 +216,22 @@ def vbm_cross_taps(grid: Grid, taps, resolver: int = RESOLVE_CACHED, stream=None
     import torch
     check(load().vbm_cross_taps(grid.handle, _dev_ptr(taps, torch.int32, (grid.n + 1) * CROSS_TAPS, "taps"),
                                 int(resolver), _stream_handle(stream)))
+
+
+def vbm_weno_filter(grid: Grid, phi, out, iso: float = 0.0, resolver: int = RESOLVE_CACHED, stream=None) -> None:
+    """19-tap WENO consumer (Godunov squared gradient norm) of an N+1 float32
+    CUDA tensor phi (row 0 the background value) into out (N+1 float32)."""
+    import torch
+    m = grid.n + 1
+    check(load().vbm_weno_filter(grid.handle, _dev_ptr(phi, torch.float32, m, "phi"), float(iso),
+                                 _dev_ptr(out, torch.float32, m, "out"), int(resolver), _stream_handle(stream)))
+
+
+def vbm_weno_taps(grid: Grid, taps, resolver: int = RESOLVE_CACHED, stream=None) -> None:
+    """(N+1)*19 uint32 (as torch.int32) CUDA tensor of raw WENO taps."""
+    import torch
+    check(load().vbm_weno_taps(grid.handle, _dev_ptr(taps, torch.int32, (grid.n + 1) * WENO_TAPS, "taps"),
+                               int(resolver), _stream_handle(stream)))
 
 
 class HostPipeline:

@@ -91,6 +91,10 @@ def load(path: str = LIB_PATH):
             lib.vbm_box_taps.argtypes = [p, p, i32, p]
             lib.vbm_cross_taps.restype = i32
             lib.vbm_cross_taps.argtypes = [p, p, i32, p]
+            lib.vbm_weno_filter.restype = i32
+            lib.vbm_weno_filter.argtypes = [p, p, ctypes.c_float, p, i32, p]
+            lib.vbm_weno_taps.restype = i32
+            lib.vbm_weno_taps.argtypes = [p, p, i32, p]
             _lib = lib
     return _lib
 

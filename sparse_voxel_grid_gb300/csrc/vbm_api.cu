@@ -336,6 +336,29 @@ static int taps_common(const vbm_grid* g, uint32_t* taps, int resolver, void* st
     return e == cudaSuccess ? VBM_OK : fail_cuda((std::string(fn) + ": launch").c_str(), e);
 }
 
+int vbm_weno_filter(const vbm_grid* g, const float* phi, float iso, float* out, int resolver, void* stream) {
+    g_last_error.clear();
+    int rc = check_filter(g, phi, 1, out, resolver, "vbm_weno_filter");
+    if (rc) return rc;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_weno_filter: cannot select the grid's device");
+    cudaError_t e = vbm::launch_weno_filter(g->dev, phi, iso, out, resolver, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_weno_filter: launch", e);
+}
+
+int vbm_weno_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) {
+    g_last_error.clear();
+    int rc = check_grid(g, "vbm_weno_taps");
+    if (rc) return rc;
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED && resolver != VBM_RESOLVE_BRICK)
+        return fail(VBM_ERR_INVALID, "vbm_weno_taps: unknown resolver");
+    if ((rc = check_ptr(taps, "vbm_weno_taps", "taps"))) return rc;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_weno_taps: cannot select the grid's device");
+    cudaError_t e = vbm::launch_weno_taps(g->dev, taps, resolver, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_weno_taps: launch", e);
+}
+
 int vbm_box_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) {
     g_last_error.clear();
     return taps_common(g, taps, resolver, stream, true);

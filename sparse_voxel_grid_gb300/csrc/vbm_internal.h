@@ -24,6 +24,7 @@ constexpr int kUpperSlots = 32 * 32 * 32;   // children of an upper node (lower 
 constexpr int kLowerSlots = 16 * 16 * 16;   // children of a lower node (leaves)
 constexpr int kBoxTaps = 27;
 constexpr int kCrossTaps = 7;
+constexpr int kWenoTaps = 19;
 constexpr int kMaxC = 64;
 constexpr int kNbrStride = 32;              // neighbour-row stride: 27 ids + 5 pad = one 128-byte line
 

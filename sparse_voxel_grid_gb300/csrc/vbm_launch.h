@@ -19,11 +19,16 @@ cudaError_t launch_cross_filter(const DevGrid& g, const float* sidecar, int C, f
 
 cudaError_t launch_box_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream);
 cudaError_t launch_cross_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream);
+cudaError_t launch_weno_filter(const DevGrid& g, const float* phi, float iso, float* out, int resolver,
+                               cudaStream_t stream);
+cudaError_t launch_weno_taps(const DevGrid& g, uint32_t* taps, int resolver, cudaStream_t stream);
 
 // Brick resolver (vbm_brick.cu).
 cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, float* out, cudaStream_t stream);
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream);
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream);
+cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream);
+cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream);
 
 // Threads per block for a block width of 2^log2w slots (one slot per thread).
 inline int threads_for(int log2w) { return 1 << log2w; }

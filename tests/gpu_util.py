@@ -53,10 +53,18 @@ def cross_filter(g, sidecar_dev, C, resolver, op):
     return out.cpu().numpy()
 
 
+def weno_filter(g, phi_dev, resolver, iso=0.0):
+    t = torch()
+    out = t.full((g.n + 1,), float("nan"), dtype=t.float32, device="cuda")
+    vbm.vbm_weno_filter(g, phi_dev, out, iso, resolver)
+    t.cuda.synchronize()
+    return out.cpu().numpy()
+
+
 def taps(g, shape, resolver):
     t = torch()
     out = t.full(((g.n + 1) * shape,), -1, dtype=t.int32, device="cuda")
-    (vbm.vbm_box_taps if shape == 27 else vbm.vbm_cross_taps)(g, out, resolver)
+    {27: vbm.vbm_box_taps, 7: vbm.vbm_cross_taps, 19: vbm.vbm_weno_taps}[shape](g, out, resolver)
     t.cuda.synchronize()
     return out.cpu().numpy().view(np.uint32).reshape(-1, shape)
 

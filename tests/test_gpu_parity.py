@@ -109,6 +109,37 @@ def test_constant_sidecar_counts():
     assert got[0] == 0 and got[1:].min() >= 1 and got[1:].max() <= 27
 
 
+def _phi(o, seed, background=0.75):
+    rng = np.random.default_rng(seed)
+    phi = rng.standard_normal(o.n + 1).astype(np.float32)
+    phi[0] = background
+    return phi
+
+
+@pytest.mark.parametrize("log2w", [6, 7, 8, 9])
+@pytest.mark.parametrize("resolver", RESOLVERS)
+def test_weno(case, log2w, resolver):
+    _, coords, o = case
+    g = vbm.vbm_build(coords, log2w)
+    np.testing.assert_array_equal(gu.taps(g, 19, resolver), o.taps(19))
+    phi = _phi(o, seed=log2w)
+    got = gu.weno_filter(g, gu.to_dev(phi), resolver, iso=0.1)
+    np.testing.assert_array_equal(gu.bits(got), gu.bits(o.weno_filter(phi, iso=0.1)))
+
+
+@pytest.mark.parametrize("resolver", RESOLVERS)
+def test_weno_integer_field_and_ties(case, resolver):
+    # integer-valued phi: some centres equal iso exactly (the inside branch)
+    _, coords, o = case
+    g = vbm.vbm_build(coords, 7)
+    c = o.coords()
+    phi = np.zeros(o.n + 1, dtype=np.float32)
+    phi[1:] = (c[:, 0] + 2 * c[:, 1] - c[:, 2]) % 7 - 3
+    phi[0] = 5.0
+    want = o.weno_filter(phi, iso=0.0)
+    np.testing.assert_array_equal(gu.bits(gu.weno_filter(g, gu.to_dev(phi), resolver, iso=0.0)), gu.bits(want))
+
+
 def test_empty_grid():
     t = gu.torch()
     g = vbm.vbm_build(np.zeros((0, 3), dtype=np.int32), 7)
@@ -120,6 +151,12 @@ def test_empty_grid():
     taps = t.full((27,), 9, dtype=t.int32, device="cuda")
     vbm.vbm_box_taps(g, taps)
     lib = vbm.load()
+    wout = t.full((1,), 5.0, device="cuda")
+    vbm.vbm_weno_filter(g, s[:1], wout, 0.0, vbm.RESOLVE_BRICK)
+    wtaps = t.full((19,), 9, dtype=t.int32, device="cuda")
+    vbm.vbm_weno_taps(g, wtaps)
+    t.cuda.synchronize()
+    assert (wout.cpu() == 0).all() and (wtaps.cpu() == 0).all()
     assert lib.vbm_decode(g.handle, None, None, None) == 0  # no slots: nothing to write
     assert lib.vbm_decode_sweep(g.handle, None, None, None) == 0
     t.cuda.synchronize()
@@ -145,6 +182,11 @@ def test_device_errors():
     assert lib.vbm_box_filter(g.handle, ok, 1, mis, 7, 0, None) == -1
     assert lib.vbm_cross_filter(g.handle, ok, 1, ok2, 1, 5, None) == -1
     assert b"op" in lib.vbm_last_error()
+    assert lib.vbm_weno_filter(g.handle, mis, 0.0, ok2, 1, None) == -6
+    assert lib.vbm_weno_filter(g.handle, ok, 0.0, ok, 1, None) == -1  # aliasing
+    assert lib.vbm_weno_filter(g.handle, ok, 0.0, ok2, 9, None) == -1
+    assert lib.vbm_weno_taps(g.handle, ok, 9, None) == -1
+    assert lib.vbm_weno_taps(g.handle, None, 0, None) == -1
     for fn in (lib.vbm_decode, lib.vbm_decode_sweep):
         assert fn(g.handle, None, ok, None) == -1
         assert fn(g.handle, mis, ok, None) == -6

@@ -94,6 +94,32 @@ def test_shell_laplacian(shell):
             np.testing.assert_array_equal(got, want, err_msg=f"W=2^{log2w} resolver={r}")
 
 
+def _level_set(o, background=3.0):
+    """phi = |p| - 185 (the shell's signed distance), row 0 the background."""
+    c = o.coords().astype(np.float64)
+    phi = np.empty(o.n + 1, dtype=np.float32)
+    phi[1:] = (np.sqrt((c ** 2).sum(1)) - 185.0).astype(np.float32)
+    phi[0] = background
+    return phi
+
+
+def test_shell_weno(shell):
+    coords, o = shell
+    phi = _level_set(o)
+    want = gu.bits(o.weno_filter(phi, iso=0.0))
+    pd = gu.to_dev(phi)
+    for log2w in (6, 7, 8, 9):
+        g = vbm.vbm_build(coords, log2w)
+        for r in RESOLVERS:
+            got = gu.bits(gu.weno_filter(g, pd, r, iso=0.0))
+            np.testing.assert_array_equal(got, want, err_msg=f"W=2^{log2w} resolver={r}")
+        if log2w in (7, 9):
+            taps = gu.taps(g, 19, vbm.RESOLVE_BRICK)
+            np.testing.assert_array_equal(taps, gu.taps(g, 19, vbm.RESOLVE_CACHED))
+            which = _sample(o.n, k=5000, seed=log2w)
+            np.testing.assert_array_equal(taps[which], o.taps(19, which=which))
+
+
 @pytest.fixture(scope="module")
 def bricks():
     coords = synth.WORKLOADS["D"]()
@@ -130,3 +156,17 @@ def test_fog_box_filter():
     which = _sample(o.n, k=6000)
     want = gu.bits(o.box_filter(s, C, which=which)).reshape(-1, C)
     np.testing.assert_array_equal(cached.reshape(-1, C)[which], want)
+
+
+def test_fog_weno():
+    coords = synth.WORKLOADS["F"]()
+    o = oracle.OracleGrid(coords)
+    g = vbm.vbm_build(coords, 8)
+    phi = synth.sidecar_normal(o.n, 1, seed=3)
+    phi[0] = 0.5
+    pd = gu.to_dev(phi)
+    cached = gu.bits(gu.weno_filter(g, pd, vbm.RESOLVE_CACHED))
+    np.testing.assert_array_equal(gu.bits(gu.weno_filter(g, pd, vbm.RESOLVE_BRICK)), cached)
+    np.testing.assert_array_equal(gu.bits(gu.weno_filter(g, pd, vbm.RESOLVE_TREEWALK)), cached)
+    which = _sample(o.n, k=6000, seed=3)
+    np.testing.assert_array_equal(cached[which], gu.bits(o.weno_filter(phi, which=which)))
