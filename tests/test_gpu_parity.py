@@ -140,6 +140,27 @@ def test_weno_integer_field_and_ties(case, resolver):
     np.testing.assert_array_equal(gu.bits(gu.weno_filter(g, gu.to_dev(phi), resolver, iso=0.0)), gu.bits(want))
 
 
+@pytest.mark.parametrize("C", [8, 16, 24])
+def test_box_16_byte_aligned_buffers(C):
+    # sidecar and output 16- but not 32-byte aligned: the float4 lanes run
+    # instead of the 256-bit ones, with the same bits
+    t = gu.torch()
+    coords = SMALL["tiny_shell"]()
+    o = oracle.OracleGrid(coords)
+    g = vbm.vbm_build(coords, 7)
+    s = synth.sidecar_uniform(o.n, C, seed=2)
+    want = gu.bits(o.box_filter(s, C))
+    m = (o.n + 1) * C
+    sbuf = t.zeros(m + 8, dtype=t.float32, device="cuda")
+    obuf = t.full((m + 8,), float("nan"), dtype=t.float32, device="cuda")
+    assert sbuf.data_ptr() % 32 == 0 and obuf.data_ptr() % 32 == 0
+    for shift in (0, 4):
+        sbuf[shift:shift + m] = t.from_numpy(s).cuda()
+        vbm.vbm_box_filter(g, sbuf[shift:shift + m], C, obuf[shift:shift + m], vbm.RESOLVE_BRICK)
+        t.cuda.synchronize()
+        np.testing.assert_array_equal(gu.bits(obuf[shift:shift + m].cpu().numpy()), want)
+
+
 def test_empty_grid():
     t = gu.torch()
     g = vbm.vbm_build(np.zeros((0, 3), dtype=np.int32), 7)
