@@ -34,7 +34,13 @@ sys.path.insert(0, ROOT)
 CS = (1, 3, 8, 16)
 LOG2W = 9
 METRIC = "active voxels/s (27-tap box filter, C=1..16) and achieved HBM GB/s vs GB300 peak"
-WORKLOAD = "S185 sphere shell 183.5<=|p|<=186.5"
+WORKLOADS = {
+    "T": "T tiny sphere shell 11.5<=|p|<=13.5",
+    "S185": "S185 sphere shell 183.5<=|p|<=186.5",
+    "S160": "S160 sphere shell 158<=|p|<=162 (the pages' shell counts)",
+    "D": "D random 8^3 bricks on [0,512)^3 (leaf p=0.3, density U[0.01,1])",
+    "F": "F 4-octave value-noise fog on [0,512)^3 (> 0.55)",
+}
 LEAF_META_BYTES = 88  # mask 64 + 9-bit directory 8 + first index 4 + origin 12
 
 
@@ -145,8 +151,8 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    coords = synth.WORKLOADS["S185"]()
-    g = vbm.vbm_build(coords, args.log2w)
+    coords = synth.WORKLOADS[args.workload]()
+    g = vbm.vbm_build_device(torch.from_numpy(coords).cuda(), args.log2w)
     info = g.info
     n, W = info["n_active"], info["block_width"]
     stream = torch.cuda.current_stream()
@@ -220,19 +226,15 @@ def run_gpu(args):
     variants = run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args) if not args.no_variants else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(coords, sample=args.cpu_sample)
+        cpu = cpu_baseline(coords, sample=args.cpu_sample, workload=args.workload)
 
     clk = clocks.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": f"{WORKLOAD}, N={n}, leaves={info['n_leaves']}, fused decode + {args.resolver} "
-                               f"resolver + streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
-                   "n_active": n, "n_leaves": info["n_leaves"], "block_width": W, "channels": list(CS),
-                   "resolver": args.resolver, "output": "streamed", "l2": "flushed before every launch",
-                   "value_counts": "4*N voxels per step (one per channel width)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(args, n, info["n_leaves"], info["n_blocks"], info["n_blocks_over_cache"],
+                                  info["max_span"], world),
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
         "roofline": {"bound": "hbm", "kernel": f"box filter ({args.resolver} resolver, streamed) C={dom}", "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
@@ -249,6 +251,17 @@ def run_gpu(args):
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def workload_config(args, n, n_leaves, n_blocks, n_over, max_span, world):
+    """The `config` object both arms print for the same workload."""
+    W = 1 << args.log2w
+    return {"workload": f"{WORKLOADS[args.workload]}, N={n}, leaves={n_leaves}, fused decode + {args.resolver} "
+                        f"resolver + streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
+            "n_active": n, "n_leaves": n_leaves, "block_width": W, "channels": list(CS), "n_blocks": n_blocks,
+            "n_blocks_over_cache": n_over, "max_span": max_span, "resolver": args.resolver, "output": "streamed",
+            "l2": "flushed before every launch", "value_counts": "4*N voxels per step (one per channel width)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def load_traffic(key):
@@ -357,12 +370,12 @@ def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):
 
 def _oracle_box_worker(task):
     """One host process of the all-cores oracle timing: the box filter of
-    voxels [lo, hi) of the shell at every channel width, compute time only."""
-    lo, hi = task
+    voxels [lo, hi) of the workload at every channel width, compute time only."""
+    workload, lo, hi = task
     import oracle
     import synth
 
-    o = oracle.OracleGrid(synth.WORKLOADS["S185"]())
+    o = oracle.OracleGrid(synth.WORKLOADS[workload]())
     sides = {C: synth.sidecar_uniform(o.n, C, seed=0) for C in CS}
     which = np.arange(lo, hi, dtype=np.int64)
     t0 = time.perf_counter()
@@ -371,14 +384,15 @@ def _oracle_box_worker(task):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(coords, sample, procs=None):
+def cpu_baseline(coords, sample, workload="S185", procs=None, per_process=100_000):
     """The oracle, as it stands, on the host cores.
 
     - Single process: the stages timed separately (index build, decode of
       every slot, box filter at each C and the Laplacian on a sample).
     - All cores: the unmodified single-threaded oracle in one spawned process
-      per core, each filtering a disjoint slice of the shell; the value counts
-      the voxels of all slices over the slowest process's compute time.
+      per core, each filtering a disjoint slice of the first
+      min(N, cores * per_process) voxels; the value counts the voxels of all
+      slices over the slowest process's compute time.
     """
     import multiprocessing as mp
 
@@ -408,18 +422,22 @@ def cpu_baseline(coords, sample, procs=None):
     single = len(CS) * len(which) / t
 
     procs = procs or max(1, os.cpu_count() or 1)
-    per = -(-o.n // procs)
-    tasks = [(1 + i * per, min(o.n, (i + 1) * per) + 1) for i in range(procs) if 1 + i * per <= o.n]
+    # each process holds the whole grid and its sidecars (~160 B per voxel):
+    # keep the total under ~24 GB of host memory
+    procs = max(1, min(procs, int(24e9 // max(1, 160 * o.n))))
+    m = min(o.n, procs * per_process)
+    per = -(-m // procs)
+    tasks = [(workload, 1 + i * per, min(m, (i + 1) * per) + 1) for i in range(procs) if 1 + i * per <= m]
     with mp.get_context("spawn").Pool(len(tasks)) as pool:
         times = pool.map_async(_oracle_box_worker, tasks).get(timeout=600)
-    all_cores = len(CS) * o.n / max(times)
+    all_cores = len(CS) * m / max(times)
     return {"value": all_cores, "unit": "voxels/s", "cores": len(tasks), "kind": "oracle",
-            "sample": f"all {o.n} voxels of the shell at C=1,3,8,16, split into {len(tasks)} slices, one "
+            "sample": f"the first {m} of {o.n} voxels at C=1,3,8,16, split into {len(tasks)} slices, one "
                       f"spawned process per core running the single-threaded C++ oracle (index build and "
                       f"sidecar generation in each process not counted)",
             "seconds": max(times),
             "single_core": {"value": single, "cores": 1,
-                            "sample": f"first {len(which)} voxels of the shell at C=1,3,8,16", "seconds": t},
+                            "sample": f"first {len(which)} voxels at C=1,3,8,16", "seconds": t},
             "stages_single_core": stages}
 
 
@@ -430,7 +448,7 @@ def run_reference(args):
     import oracle
     import synth
 
-    coords = synth.WORKLOADS["S185"]()
+    coords = synth.WORKLOADS[args.workload]()
     o = oracle.OracleGrid(coords)
     sides = {C: synth.sidecar_uniform(o.n, C, seed=0) for C in CS}
     # Size the per-step sample so that warm-up + timed steps take about
@@ -455,13 +473,17 @@ def run_reference(args):
         step()
     dt = (time.perf_counter() - t0) / args.steps
     value = len(CS) * len(which) / dt
-    sample = f"first {len(which)} of {o.n} voxels of the shell per step, C=1,3,8,16 (single-threaded C++ oracle)"
+    sample = f"first {len(which)} of {o.n} voxels per step, C=1,3,8,16 (single-threaded C++ oracle)"
+    _, origins = o.leaves()
+    fl, jm = o.blocks(args.log2w)
+    spans = 1 + np.array([sum(bin(int(w)).count("1") for w in row) for row in jm], dtype=np.int64)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
-        "config": {"workload": f"{WORKLOAD}, N={o.n}, 27-tap box filter at C=1,3,8,16", "n_active": o.n,
-                   "channels": list(CS), "sample_voxels": len(which)},
+        "config": {**workload_config(args, o.n, len(origins), len(fl), int((spans > 16).sum()),
+                                     int(spans.max()) if len(spans) else 0, world),
+                   "sample_voxels": len(which)},
         "cpu_baseline": {"value": value, "unit": "voxels/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -526,6 +548,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--resolver", choices=["cached", "brick", "walk"], default="brick")
     ap.add_argument("--log2w", type=int, default=LOG2W, choices=[6, 7, 8, 9])
+    ap.add_argument("--workload", default="S185", choices=sorted(WORKLOADS),
+                    help="input grid (default: the S185 shell, the headline workload)")
     ap.add_argument("--cpu-sample", type=int, default=150000)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--variant-reps", type=int, default=5)
