@@ -27,8 +27,18 @@ def _exact_blocks(n=256):
     return c[:n]
 
 
+def _extreme():
+    # at the builder's coordinate bound +-2^30, with full stencils around them
+    lim = 2 ** 30
+    parts = [synth.dense_random((6, 5, 7), 0.6, seed=11, origin=(lim - 5, -lim, lim - 6)),
+             synth.dense_random((5, 6, 5), 0.6, seed=12, origin=(-lim, lim - 5, -3)),
+             np.array([[lim, lim, lim], [-lim, -lim, -lim], [0, 0, 0]], dtype=np.int32)]
+    return np.unique(np.concatenate(parts), axis=0).astype(np.int32)
+
+
 SMALL = dict(GRIDS)
 SMALL.update({
+    "extreme": _extreme,
     "scatter": lambda: synth.scatter(side=10, count=700, origin=-37, seed=5),
     "single": _single,
     "exact_blocks": _exact_blocks,
@@ -82,6 +92,23 @@ def test_box_filter_all_variants(case, C):
             for out in (OUTPUTS if r != vbm.RESOLVE_BRICK else OUTPUTS[:1]):
                 got = gu.bits(gu.box_filter(g, sd, C, r, out))
                 np.testing.assert_array_equal(got, want, err_msg=f"W=2^{log2w} resolver={r} output={out}")
+
+
+@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("name", ["tiny_shell", "clusters"])
+def test_wide_channels(name, C):
+    # the widest sidecars (64 channels is the maximum C)
+    coords = SMALL[name]()
+    o = oracle.OracleGrid(coords)
+    s = synth.sidecar_uniform(o.n, C, seed=C)
+    sd = gu.to_dev(s)
+    want = gu.bits(o.box_filter(s, C))
+    want_lap = gu.bits(o.cross_filter(s, C, op=vbm.CROSS_LAPLACIAN))
+    for log2w in (6, 9):
+        g = vbm.vbm_build(coords, log2w)
+        for r in RESOLVERS:
+            np.testing.assert_array_equal(gu.bits(gu.box_filter(g, sd, C, r, vbm.OUTPUT_STREAMED)), want)
+            np.testing.assert_array_equal(gu.bits(gu.cross_filter(g, sd, C, r, vbm.CROSS_LAPLACIAN)), want_lap)
 
 
 @pytest.mark.parametrize("C", [1, 3, 8, 16])
