@@ -373,7 +373,10 @@ constexpr int kWEdge = 14;
 constexpr int kWCells = kWEdge * kWEdge * kWEdge;
 constexpr int kWRows = 64 + 48 + 48;
 
-__host__ __device__ constexpr int weno_group(int log2w) { return log2w <= 7 ? 2 : log2w == 8 ? 3 : 4; }
+// Leaves whose WENO bricks are built per round, by block width: about the
+// leaves a block spans on the shell (a 64-slot block rarely spans two), within
+// shared memory that keeps two 512-thread CTAs per SM.
+__host__ __device__ constexpr int weno_group(int log2w) { return log2w <= 6 ? 1 : log2w == 7 ? 2 : log2w == 8 ? 3 : 6; }
 
 __host__ __device__ constexpr size_t weno_smem_bytes(int log2w) {
     return (size_t)weno_group(log2w) * kWCells * sizeof(uint32_t) + (size_t)3 * ((1u << log2w) + 1) * sizeof(uint16_t);
@@ -554,13 +557,26 @@ cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, fl
                                      : launch_brick_kind<2>(g, sidecar, C, out, stream);
 }
 
+// Dynamic shared memory above the default 48 KB needs an opt-in per kernel
+// (set on the current device at every launch that needs it).
+template <bool TAPS>
+cudaError_t weno_smem_opt_in(int log2w) {
+    const size_t bytes = weno_smem_bytes(log2w);
+    if (bytes <= 48u * 1024u) return cudaSuccess;
+    return cudaFuncSetAttribute(brick_weno_kernel<TAPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream) {
+    const cudaError_t e = weno_smem_opt_in<false>(g.log2w);
+    if (e != cudaSuccess) return e;
     brick_weno_kernel<false><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, phi, iso, out,
                                                                                                       nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream) {
+    const cudaError_t e = weno_smem_opt_in<true>(g.log2w);
+    if (e != cudaSuccess) return e;
     brick_weno_kernel<true><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, nullptr, 0.0f,
                                                                                                      nullptr, taps);
     return cudaGetLastError();
