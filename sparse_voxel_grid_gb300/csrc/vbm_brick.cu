@@ -36,12 +36,15 @@
 // same order, so the results are identical bit for bit.  There is no
 // MaxCachedLeaves limit: blocks spanning more than kMaxGroup leaves are built
 // in several rounds.
+#include "vbm_brick.cuh"
 #include "vbm_launch.h"
 #include "vbm_stencil.cuh"
-#include "vbm_weno.cuh"
 
 namespace vbm {
 namespace {
+
+using brick::BrickCtx;
+using brick::brick_prologue;
 
 constexpr int kEdge = 10;  // brick edge: leaf-relative -1..8
 constexpr int kCells = kEdge * kEdge * kEdge;
@@ -49,6 +52,12 @@ constexpr int kCells = kEdge * kEdge * kEdge;
 // Leaves whose bricks are built in one round, by block width (shared memory
 // kMaxGroup * 4000 bytes).
 __host__ __device__ constexpr int max_group(int log2w) { return log2w <= 7 ? 4 : log2w == 8 ? 6 : 8; }
+
+// Dynamic shared memory: ib[group][1000] index bricks, then offs[W] (voxel
+// offset of each slot), lof[W] (slot's leaf - firstLeafID) and starts[span+1].
+__host__ __device__ constexpr size_t brick_smem_bytes(int log2w) {
+    return (size_t)max_group(log2w) * kCells * sizeof(uint32_t) + (size_t)3 * ((1u << log2w) + 1) * sizeof(uint16_t);
+}
 
 // The 10 indices of brick row (bx, by) of the leaf whose neighbour row is
 // `nrow` (27 leaf ids at (dx+1)*9 + (dy+1)*3 + (dz+1)).  Cell k holds
@@ -83,94 +92,6 @@ __device__ __forceinline__ int own_cell(uint32_t off) {
 
 __device__ __forceinline__ constexpr int box_cell_delta(int t) { return (t / 9 - 1) * 100 + ((t / 3) % 3 - 1) * 10 + (t % 3 - 1); }
 __device__ __forceinline__ constexpr int cross_cell_delta(int j) { return cross_di(j) * 100 + cross_dj(j) * 10 + cross_dk(j); }
-
-// Per-block state.  Shared memory (dynamic): ib[group][1000] index bricks,
-// then offs[W] (voxel offset of each slot), lof[W] (slot's leaf - firstLeafID)
-// and starts[span+1] (first slot of each spanned leaf; starts[span] = valid
-// slots).
-struct BrickCtx {
-    uint32_t b, W, fl, span, n_valid;
-    const uint64_t* jb;
-};
-
-__host__ __device__ constexpr size_t brick_smem_bytes(int log2w) {
-    return (size_t)max_group(log2w) * kCells * sizeof(uint32_t) + (size_t)3 * ((1u << log2w) + 1) * sizeof(uint16_t);
-}
-
-// Decode every valid slot of the block (select-based decode, [2258] "What
-// changed") into offs/lof and record where each spanned leaf starts.  Ends with
-// a barrier.
-__device__ __forceinline__ void brick_prologue_direct(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
-    k.W = 1u << g.log2w;
-    const uint32_t words = k.W >> 6;
-    k.b = blockIdx.x;
-    k.jb = g.jump + (size_t)k.b * words;
-    k.fl = __ldg(&g.first_leaf[k.b]);
-    k.span = block_span(k.jb, words);
-    k.n_valid = min(k.W, g.n - k.b * k.W);
-    for (uint32_t s = threadIdx.x; s < k.n_valid; s += blockDim.x) {
-        const Slot d = decode_slot(g, k.fl, k.jb, s, 1u + k.b * k.W + s);
-        offs[s] = (uint16_t)d.off;
-        lof[s] = (uint16_t)(d.leaf - k.fl);
-        if (s == 0 || ((__ldg(&k.jb[s >> 6]) >> (s & 63u)) & 1ull)) starts[d.leaf - k.fl] = (uint16_t)s;
-    }
-    if (threadIdx.x == 0) starts[k.span] = (uint16_t)k.n_valid;
-    __syncthreads();
-}
-
-__device__ __forceinline__ void brick_prologue_staged(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
-    // The block's jumpMap words and their popcount prefixes, staged once.
-    __shared__ uint64_t s_jw[8];
-    __shared__ uint32_t s_cum[9];
-    k.W = 1u << g.log2w;
-    const uint32_t words = k.W >> 6;
-    k.b = blockIdx.x;
-    k.jb = g.jump + (size_t)k.b * words;
-    k.fl = __ldg(&g.first_leaf[k.b]);
-    k.n_valid = min(k.W, g.n - k.b * k.W);
-    if (threadIdx.x < 32u) {
-        const uint32_t lane = threadIdx.x;
-        const uint64_t w = lane < words ? __ldg(&k.jb[lane]) : 0ull;
-        const uint32_t c = (uint32_t)__popcll(w);
-        uint32_t incl = c;
-#pragma unroll
-        for (int d = 1; d < 8; d <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= (uint32_t)d) incl += t;
-        }
-        if (lane < words) {
-            s_jw[lane] = w;
-            s_cum[lane] = incl - c;
-        }
-        if (lane == words - 1u) s_cum[words] = incl;
-    }
-    __syncthreads();
-    k.span = 1u + s_cum[words];
-    for (uint32_t s = threadIdx.x; s < k.n_valid; s += blockDim.x) {
-        const uint32_t ws = s >> 6;
-        const uint64_t jw = s_jw[ws];
-        const uint32_t leaf = k.fl + s_cum[ws] + (uint32_t)__popcll(jw & ((2ull << (s & 63u)) - 1ull));
-        const LeafRec* rec = g.leaves + leaf;
-        const uint32_t off = leaf_select(rec, 1u + k.b * k.W + s - __ldg(&rec->first));
-        offs[s] = (uint16_t)off;
-        lof[s] = (uint16_t)(leaf - k.fl);
-        if (s == 0 || ((jw >> (s & 63u)) & 1ull)) starts[leaf - k.fl] = (uint16_t)s;
-    }
-    if (threadIdx.x == 0) starts[k.span] = (uint16_t)k.n_valid;
-    __syncthreads();
-}
-
-// STAGED: jumpMap words and popcount prefixes in shared memory (faster for
-// the one-lane layouts); otherwise each thread ranks from global memory
-// (measured faster for the float4-lane layouts).
-template <bool STAGED>
-__device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
-    if constexpr (STAGED) brick_prologue_staged(g, k, offs, lof, starts);
-    else brick_prologue_direct(g, k, offs, lof, starts);
-}
 
 // Build the bricks of spanned leaves l0 .. l0+nb-1 into ib[0..nb).  Leaf l's
 // voxels in this block run from slot starts[l] to starts[l+1]-1, in increasing
@@ -359,165 +280,6 @@ __global__ void __launch_bounds__(512) brick_taps_kernel(DevGrid g, uint32_t* __
     if (blockIdx.x == 0 && threadIdx.x < (unsigned)SHAPE) taps[threadIdx.x] = 0u;
 }
 
-// ---------------------------------------------------------------------------
-// 19-tap WENO through bricks.  The WENO taps reach 3 steps along one axis, so
-// a leaf's brick is a 14x14x14 box (leaf-relative -3..10 on each axis) of
-// which only the cells a tap can reach are filled: the 64 core z-rows (x, y in
-// 0..7; z in -3..10) and the 48 + 48 rows of the x and y face slabs (one of
-// x, y in -3..-1 or 8..10, the other in 0..7; z in 0..7).  Cells hold
-// phi[idx] (VALUES; an inactive cell holds phi[0], the background) or idx.
-// Only rows whose x lies within 3 of the x range of the block's voxels of that
-// leaf are built.
-// ---------------------------------------------------------------------------
-constexpr int kWEdge = 14;
-constexpr int kWCells = kWEdge * kWEdge * kWEdge;
-constexpr int kWRows = 64 + 48 + 48;
-
-// Leaves whose WENO bricks are built per round, by block width: about the
-// leaves a block spans on the shell (a 64-slot block rarely spans two), within
-// shared memory that keeps two 512-thread CTAs per SM.
-__host__ __device__ constexpr int weno_group(int log2w) { return log2w <= 6 ? 1 : log2w == 7 ? 2 : log2w == 8 ? 3 : 6; }
-
-__host__ __device__ constexpr size_t weno_smem_bytes(int log2w) {
-    return (size_t)weno_group(log2w) * kWCells * sizeof(uint32_t) + (size_t)3 * ((1u << log2w) + 1) * sizeof(uint16_t);
-}
-
-__device__ __forceinline__ constexpr int wcell(int x, int y, int z) { return (x + 3) * 196 + (y + 3) * 14 + (z + 3); }
-
-__device__ __forceinline__ constexpr int weno_cell_delta(int j) {
-    return weno_axis(j) == 0 ? weno_step(j) * 196 : weno_axis(j) == 1 ? weno_step(j) * 14 : weno_step(j);
-}
-
-// Row r of a leaf's WENO brick -> its leaf-relative (x, y).
-__device__ __forceinline__ void weno_row_xy(uint32_t r, int& x, int& y) {
-    if (r < 64u) {
-        x = (int)(r >> 3);
-        y = (int)(r & 7u);
-    } else if (r < 112u) {
-        const int q = (int)(r - 64u), a = q >> 3;
-        x = a < 3 ? a - 3 : a + 5;
-        y = q & 7;
-    } else {
-        const int q = (int)(r - 112u), a = q >> 3;
-        y = a < 3 ? a - 3 : a + 5;
-        x = q & 7;
-    }
-}
-
-// Indices of leaf L's cells (x&7, y&7, 0..7) (0 where inactive or L is kNone).
-__device__ __forceinline__ void row_indices8(const LeafRec* __restrict__ leaves, uint32_t L, int x, int y,
-                                             uint32_t (&idx)[8]) {
-    uint32_t byte = 0, rb = 0;
-    if (L != kNone) {
-        const LeafRec* r = leaves + L;
-        const uint32_t xw = (uint32_t)(x & 7), yb = (uint32_t)(y & 7) * 8u;
-        const uint64_t word = __ldg(&r->mask[xw]);
-        byte = (uint32_t)(word >> yb) & 0xFFu;
-        rb = __ldg(&r->base[xw]) + (uint32_t)__popcll(word & ((1ull << yb) - 1ull));
-    }
-#pragma unroll
-    for (int z = 0; z < 8; ++z) idx[z] = ((byte >> z) & 1u) ? rb + (uint32_t)__popc(byte & ((1u << z) - 1u)) : 0u;
-}
-
-template <bool VALUES>
-__device__ __forceinline__ void weno_build_round(const DevGrid& g, const BrickCtx& k, const uint16_t* offs,
-                                                 const uint16_t* starts, uint32_t l0, uint32_t nb, uint32_t* wb,
-                                                 const float* __restrict__ phi) {
-    for (uint32_t e = threadIdx.x; e < nb * (uint32_t)kWRows; e += blockDim.x) {
-        const uint32_t kk = e / (uint32_t)kWRows, r = e - kk * (uint32_t)kWRows, l = l0 + kk;
-        int x, y;
-        weno_row_xy(r, x, y);
-        const int x0 = (int)(offs[starts[l]] >> 6), x1 = (int)(offs[starts[l + 1] - 1u] >> 6);
-        if (x < x0 - 3 || x > x1 + 3) continue;
-        const uint32_t* nrow = g.nbr + (size_t)(k.fl + l) * kNbrStride;
-        const int sx = x < 0 ? 0 : x > 7 ? 2 : 1, sy = y < 0 ? 0 : y > 7 ? 2 : 1;
-        uint32_t idx[8];
-        row_indices8(g.leaves, __ldg(nrow + sx * 9 + sy * 3 + 1), x, y, idx);
-        uint32_t* dst = wb + kk * kWCells + wcell(x, y, 0);
-        if constexpr (VALUES) {
-#pragma unroll
-            for (int z = 0; z < 8; ++z) dst[z] = __float_as_uint(__ldg(phi + idx[z]));
-        } else {
-#pragma unroll
-            for (int z = 0; z < 8; ++z) dst[z] = idx[z];
-        }
-        if (r < 64u) {  // core row: the z halo, 3 cells from each z neighbour
-            uint32_t lo[8], hi[8];
-            row_indices8(g.leaves, __ldg(nrow + 12), x, y, lo);
-            row_indices8(g.leaves, __ldg(nrow + 14), x, y, hi);
-            if constexpr (VALUES) {
-#pragma unroll
-                for (int z = 0; z < 3; ++z) {
-                    dst[z - 3] = __float_as_uint(__ldg(phi + lo[5 + z]));
-                    dst[8 + z] = __float_as_uint(__ldg(phi + hi[z]));
-                }
-            } else {
-#pragma unroll
-                for (int z = 0; z < 3; ++z) {
-                    dst[z - 3] = lo[5 + z];
-                    dst[8 + z] = hi[z];
-                }
-            }
-        }
-    }
-    __syncthreads();
-}
-
-struct WenoSmem {
-    uint32_t* wb;
-    uint16_t *offs, *lof, *starts;
-    uint32_t group;
-};
-
-__device__ __forceinline__ WenoSmem carve_weno(unsigned char* smem, int log2w) {
-    WenoSmem m;
-    const uint32_t W1 = (1u << log2w) + 1u;
-    m.group = (uint32_t)weno_group(log2w);
-    m.wb = reinterpret_cast<uint32_t*>(smem);
-    m.offs = reinterpret_cast<uint16_t*>(m.wb + m.group * kWCells);
-    m.lof = m.offs + W1;
-    m.starts = m.lof + W1;
-    return m;
-}
-
-// TAPS: write the raw indices instead of the WENO value.
-template <bool TAPS>
-__global__ void __launch_bounds__(512) brick_weno_kernel(DevGrid g, const float* __restrict__ phi, float iso,
-                                                         float* __restrict__ out, uint32_t* __restrict__ taps) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    const WenoSmem m = carve_weno(smem, g.log2w);
-    BrickCtx k;
-    brick_prologue<true>(g, k, m.offs, m.lof, m.starts);
-    for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
-        const uint32_t nb = min(m.group, k.span - l0);
-        weno_build_round<!TAPS>(g, k, m.offs, m.starts, l0, nb, m.wb, phi);
-        for (uint32_t s = m.starts[l0] + threadIdx.x; s < m.starts[l0 + nb]; s += blockDim.x) {
-            const uint32_t* wbk = m.wb + (uint32_t)(m.lof[s] - l0) * kWCells;
-            const uint32_t off = m.offs[s];
-            const int cc = wcell((int)(off >> 6), (int)((off >> 3) & 7u), (int)(off & 7u));
-            const uint32_t index = 1u + k.b * k.W + s;
-            if constexpr (TAPS) {
-                uint32_t* row = taps + (size_t)index * kWenoTaps;
-#pragma unroll
-                for (int j = 0; j < kWenoTaps; ++j) row[j] = wbk[cc + weno_cell_delta(j)];
-            } else {
-                float v[kWenoTaps];
-#pragma unroll
-                for (int j = 0; j < kWenoTaps; ++j) v[j] = __uint_as_float(wbk[cc + weno_cell_delta(j)]);
-                out[index] = weno_value(v, iso);
-            }
-        }
-        __syncthreads();  // the next round overwrites the bricks
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        if constexpr (TAPS) {
-            for (int j = 0; j < kWenoTaps; ++j) taps[j] = 0u;
-        } else {
-            out[0] = 0.0f;
-        }
-    }
-}
-
 template <int KIND, int CC, bool VEC, bool VALUES, int CT = 0>
 cudaError_t launch_brick(const DevGrid& g, const float* sc, int C, int lanes, float* out, cudaStream_t stream) {
     brick_filter_kernel<KIND, CC, VEC, VALUES, CT>
@@ -555,31 +317,6 @@ cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, floa
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream) {
     return op == VBM_CROSS_LAPLACIAN ? launch_brick_kind<1>(g, sidecar, C, out, stream)
                                      : launch_brick_kind<2>(g, sidecar, C, out, stream);
-}
-
-// Dynamic shared memory above the default 48 KB needs an opt-in per kernel
-// (set on the current device at every launch that needs it).
-template <bool TAPS>
-cudaError_t weno_smem_opt_in(int log2w) {
-    const size_t bytes = weno_smem_bytes(log2w);
-    if (bytes <= 48u * 1024u) return cudaSuccess;
-    return cudaFuncSetAttribute(brick_weno_kernel<TAPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
-cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream) {
-    const cudaError_t e = weno_smem_opt_in<false>(g.log2w);
-    if (e != cudaSuccess) return e;
-    brick_weno_kernel<false><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, phi, iso, out,
-                                                                                                      nullptr);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream) {
-    const cudaError_t e = weno_smem_opt_in<true>(g.log2w);
-    if (e != cudaSuccess) return e;
-    brick_weno_kernel<true><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, nullptr, 0.0f,
-                                                                                                     nullptr, taps);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream) {
