@@ -50,8 +50,11 @@ constexpr int kEdge = 10;  // brick edge: leaf-relative -1..8
 constexpr int kCells = kEdge * kEdge * kEdge;
 
 // Leaves whose bricks are built in one round, by block width (shared memory
-// kMaxGroup * 4000 bytes).
-__host__ __device__ constexpr int max_group(int log2w) { return log2w <= 7 ? 4 : log2w == 8 ? 6 : 8; }
+// max_group * 4000 bytes).  Measured per width on the shell: small blocks gain
+// from the shared memory left to L1 and to more resident CTAs (W=64: 2 rather
+// than 4 cut C=16 from 181 to 140 us; W=256: 4 rather than 6, 133 to 123 us);
+// at W=512 one round for the ~5.5 spanned leaves matters more (8).
+__host__ __device__ constexpr int max_group(int log2w) { return log2w <= 7 ? 2 : log2w == 8 ? 4 : 8; }
 
 // Dynamic shared memory: ib[group][1000] index bricks, then offs[W] (voxel
 // offset of each slot), lof[W] (slot's leaf - firstLeafID) and starts[span+1].
