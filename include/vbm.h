@@ -129,8 +129,9 @@ int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t 
  * leaf records, child tables, VBM block metadata and neighbour rows); the
  * result equals vbm_build's array for array.  Temporary device memory is
  * allocated and freed inside the call (about 12 bytes per voxel for the hash
- * table plus ~150 bytes per leaf); the call synchronises `stream` and also
- * keeps host copies of the grid's arrays for vbm_leaf_export.  Requires
+ * table plus ~150 bytes per leaf); the call synchronises `stream`.  The grid
+ * lives on the device only; the first vbm_leaf_export copies its arrays to the
+ * host (synchronously, once per grid).  Requires
  * |x|,|y|,|z| < 2^20 (VBM_ERR_RANGE otherwise).  Errors: as vbm_build. */
 int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
                      vbm_grid** out);
@@ -171,9 +172,12 @@ int vbm_destroy(vbm_grid* grid);
 /* Sizes and statistics of a grid.  Errors: INVALID. */
 int vbm_info(const vbm_grid* grid, vbm_info_t* info);
 
-/* Copy one of the grid's host-side arrays (see VBM_EXPORT_*) into dst, which
- * holds `bytes` bytes; the exact size is required.  Errors: INVALID, RANGE
- * (bytes differs from the array's size). */
+/* Copy one of the grid's arrays (see VBM_EXPORT_*) into the host buffer dst,
+ * which holds `bytes` bytes; the exact size is required.  For a grid built by
+ * vbm_build_device the first call copies the arrays from the device (it
+ * synchronises the device and may allocate host memory).  Errors: INVALID,
+ * RANGE (bytes differs from the array's size), STATE (a
+ * vbm_build_device_noalloc grid, which keeps no host copies), NOMEM, CUDA. */
 int vbm_leaf_export(const vbm_grid* grid, int what, void* dst, uint64_t bytes);
 
 /* Select-based inverse-map decode ([2258] "What changed"): for every slot of

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -72,6 +73,38 @@ int upload(vbm_grid* g, cudaStream_t stream) {
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);
     vbm::set_device_views(g, lay, sm_count);
+    return VBM_OK;
+}
+
+// Host copies of a device-built grid's arrays, made on first use (the build
+// itself keeps everything on the device).  Thread-safe; synchronous.
+int fill_mirrors(const vbm_grid* cg) {
+    vbm_grid* g = const_cast<vbm_grid*>(cg);
+    std::lock_guard<std::mutex> lock(g->mirror_mu);
+    if (g->mirrors_filled) return VBM_OK;
+    const vbm::ArenaLayout lay = vbm::arena_layout(g->n_leaves, g->n_upper, g->n_lower, g->n_blocks, g->log2w);
+    try {
+        g->leaves.resize(g->n_leaves);
+        g->root_keys.resize(g->n_upper);
+        g->upper.resize((size_t)g->n_upper * vbm::kUpperSlots);
+        g->lower.resize((size_t)g->n_lower * vbm::kLowerSlots);
+        g->first_leaf.resize(g->n_blocks);
+        g->jump.resize(g->n_blocks * ((1u << g->log2w) >> 6));
+        g->nbr.resize((size_t)g->n_leaves * vbm::kNbrStride);
+    } catch (const std::bad_alloc&) {
+        return fail(VBM_ERR_NOMEM, "vbm_leaf_export: out of host memory");
+    }
+    void* dst[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
+                    g->first_leaf.data(), g->jump.data(), g->nbr.data()};
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_leaf_export: cannot select the grid's device");
+    const char* base = static_cast<const char*>(g->arena);
+    for (int i = 0; i < 7; ++i) {
+        if (!lay.bytes[i]) continue;
+        const cudaError_t e = cudaMemcpy(dst[i], base + lay.off[i], lay.bytes[i], cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return fail_cuda("vbm_leaf_export: cudaMemcpy", e);
+    }
+    g->mirrors_filled = true;
     return VBM_OK;
 }
 
@@ -214,6 +247,7 @@ int vbm_leaf_export(const vbm_grid* g, int what, void* dst, uint64_t bytes) {
     g_last_error.clear();
     if (!g || (!dst && bytes)) return fail(VBM_ERR_INVALID, "vbm_leaf_export: NULL argument");
     if (!g->host_mirrors) return fail(VBM_ERR_STATE, "vbm_leaf_export: this grid keeps no host copies");
+    if (int rc = fill_mirrors(g)) return rc;
     const size_t nl = g->leaves.size();
     size_t need = 0;
     switch (what) {

@@ -16,6 +16,7 @@
 // Coordinates must satisfy |x|,|y|,|z| < 2^20 so that leaf keys fit 54 bits.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -60,32 +61,56 @@ __device__ __forceinline__ uint64_t mix64d(uint64_t z) {
     return z ^ (z >> 31);
 }
 
-// Slot of `key` in the table (inserting it when `insert`); the table always
-// has an empty slot, so the probe ends; `cap` bounds it regardless.
-__device__ __forceinline__ int64_t probe(uint64_t* keys, uint64_t mask, uint64_t key, bool insert) {
+// Slot of `key` in the table (inserting it when `insert`; *fresh tells whether
+// this call inserted it).  Linear probing from a mixed hash, stopped after
+// kMaxProbe slots: a table at most half full ends far sooner.  -1 when the key
+// is absent (lookup) or no slot was found (insert).
+constexpr uint64_t kMaxProbe = 1u << 12;
+__device__ __forceinline__ int64_t probe(uint64_t* keys, uint64_t mask, uint64_t key, bool insert,
+                                         bool* fresh = nullptr) {
     uint64_t slot = mix64d(key) & mask;
-    for (uint64_t it = 0; it <= mask; ++it) {
-        const uint64_t cur = insert ? atomicCAS((unsigned long long*)&keys[slot], (unsigned long long)kEmptyKey,
-                                                (unsigned long long)key)
-                                    : keys[slot];
-        if (cur == key || (insert && cur == kEmptyKey)) return (int64_t)slot;
+    for (uint64_t it = 0; it <= mask && it < kMaxProbe; ++it) {
+        // A slot only ever changes from empty to a key, so a plain read that
+        // shows a key is final; an empty one is settled by the compare-and-swap.
+        uint64_t cur = keys[slot];
+        if (insert && cur == kEmptyKey)
+            cur = atomicCAS((unsigned long long*)&keys[slot], (unsigned long long)kEmptyKey, (unsigned long long)key);
+        if (cur == key || (insert && cur == kEmptyKey)) {
+            if (fresh) *fresh = insert && cur == kEmptyKey;
+            return (int64_t)slot;
+        }
         if (!insert && cur == kEmptyKey) return -1;
         slot = (slot + 1) & mask;
     }
     return -1;
 }
 
-// 1. Insert leaf keys; flag coordinates out of range.
+// 1. Insert leaf keys; flag coordinates out of range (err bit 0) and failed
+// probes (bit 1).  With `count`: count the distinct keys and flag (bit 2) a
+// table past `limit` keys.
 __global__ void insert_kernel(const int32_t* __restrict__ coords, uint64_t n, uint64_t* keys, uint64_t mask,
-                              uint32_t* __restrict__ err) {
-    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
-        const int32_t x = coords[3 * i], y = coords[3 * i + 1], z = coords[3 * i + 2];
-        if (x <= -kDevCoordLimit || x >= kDevCoordLimit || y <= -kDevCoordLimit || y >= kDevCoordLimit ||
-            z <= -kDevCoordLimit || z >= kDevCoordLimit) {
-            atomicOr(err, 1u);
-            continue;
+                              uint32_t* __restrict__ err, uint32_t* __restrict__ count = nullptr,
+                              uint32_t limit = 0) {
+    // Warp-uniform loop: the lanes of a warp that hold the same leaf key insert
+    // it once (the lowest such lane).
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t w0 = blockIdx.x * (uint64_t)blockDim.x + (threadIdx.x & ~31u); w0 < n; w0 += stride) {
+        const uint64_t i = w0 + lane;
+        uint64_t key = kEmptyKey;
+        if (i < n) {
+            const int32_t x = coords[3 * i], y = coords[3 * i + 1], z = coords[3 * i + 2];
+            if (x <= -kDevCoordLimit || x >= kDevCoordLimit || y <= -kDevCoordLimit || y >= kDevCoordLimit ||
+                z <= -kDevCoordLimit || z >= kDevCoordLimit)
+                atomicOr(err, 1u);
+            else
+                key = pack_leaf(x >> 3, y >> 3, z >> 3);
         }
-        if (probe(keys, mask, pack_leaf(x >> 3, y >> 3, z >> 3), true) < 0) atomicOr(err, 2u);
+        const uint32_t peers = __match_any_sync(0xffffffffu, key);
+        if (key == kEmptyKey || lane != (uint32_t)__ffs(peers) - 1u) continue;
+        bool fresh = false;
+        if (probe(keys, mask, key, true, &fresh) < 0) atomicOr(err, 2u);
+        else if (fresh && count && atomicAdd(count, 1u) >= limit) atomicOr(err, 4u);
     }
 }
 
@@ -275,13 +300,12 @@ unsigned grid_for(uint64_t work, int sm_count) {
 
 // Stable radix sort of (key, value) pairs by the low `bits` bits of the keys;
 // the result ends in (k0, v0).
-cudaError_t radix_sort(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* v1, uint32_t* hist, uint32_t n, int bits,
-                       cudaStream_t s) {
+cudaError_t radix_sort(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* v1, uint32_t* hist, uint32_t* scan_tmp,
+                       uint32_t n, int bits, cudaStream_t s) {
     const uint32_t tiles = (n + devsort::kSortThreads - 1) / devsort::kSortThreads;
     for (int shift = 0; shift < bits; shift += 8) {
         devsort::radix_hist_kernel<<<tiles, devsort::kSortThreads, 0, s>>>(k0, n, shift, tiles, hist);
-        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, s>>>(hist, (uint64_t)tiles * devsort::kDigits,
-                                                                          nullptr);
+        devsort::scan_exclusive(hist, (uint64_t)tiles * devsort::kDigits, nullptr, scan_tmp, s);
         devsort::radix_scatter_kernel<<<tiles, devsort::kSortThreads, 0, s>>>(k0, v0, k1, v1, n, shift, tiles, hist);
         std::swap(k0, k1);
         std::swap(v0, v1);
@@ -324,21 +348,34 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     const uint32_t W = 1u << log2w, words = W >> 6;
     Scratch sc;
 
-    // 1-2. Leaf hash table (capacity a power of two >= 2n) and compaction.
+    // 1-2. Leaf hash table and compaction.  The table is first sized for one
+    // leaf per 16 voxels (power of two, at most half full); a grid with more
+    // leaves than that is rebuilt once in a table of 2n slots, which no input
+    // can fill past half.
+    uint64_t full = 1024;
+    while (full < 2 * n) full <<= 1;
     uint64_t cap = 1024;
-    while (cap < 2 * n) cap <<= 1;
+    while (cap < 2 * (n / 16 + 1024)) cap <<= 1;
+    if (cap > full) cap = full;
     uint64_t* keys;
     uint32_t *slot_id, *ctr;  // ctr: [0] error flags, [1] leaves, [2] repeats, [3..4] span stats, [5..7] totals
-    VBM_CK(sc.alloc(&keys, cap));
-    VBM_CK(sc.alloc(&slot_id, cap));
     VBM_CK(sc.alloc(&ctr, 8));
-    VBM_CK(cudaMemsetAsync(keys, 0xFF, cap * sizeof(uint64_t), st));
-    VBM_CK(cudaMemsetAsync(ctr, 0, 8 * sizeof(uint32_t), st));
-    if (n) insert_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, ctr);
-    count_occupied_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, ctr + 1);
-    VBM_CK(cudaGetLastError());
     uint32_t h[2];
-    VBM_CK(read_back(h, ctr, 2, st));
+    for (;;) {
+        VBM_CK(sc.alloc(&keys, cap));
+        VBM_CK(sc.alloc(&slot_id, cap));
+        VBM_CK(cudaMemsetAsync(keys, 0xFF, cap * sizeof(uint64_t), st));
+        VBM_CK(cudaMemsetAsync(ctr, 0, 8 * sizeof(uint32_t), st));
+        if (n) insert_kernel<<<grid_for(n, sm), kThreads, 0, st>>>(coords, n, keys, cap - 1, ctr, ctr + 1,
+                                                                   (uint32_t)(cap / 2));
+        VBM_CK(cudaGetLastError());
+        VBM_CK(read_back(h, ctr, 2, st));
+        if ((h[0] & 4u) && cap < full) {
+            cap = full;  // more leaves than the first table holds
+            continue;
+        }
+        break;
+    }
     if (h[0] & 1u) {
         err = "vbm_build_device: a coordinate is outside (-2^20, 2^20)";
         return VBM_ERR_RANGE;
@@ -363,6 +400,8 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     VBM_CK(sc.alloc(&up_f, nl));
     VBM_CK(sc.alloc(&lo_f, nl));
     VBM_CK(sc.alloc(&tmask, (size_t)nl * 8u));
+    uint32_t* scan_tmp;  // tile sums of the multi-CTA scans
+    VBM_CK(sc.alloc(&scan_tmp, devsort::scan_tiles(std::max<uint64_t>(nl, (uint64_t)tiles * devsort::kDigits)) + 1u));
     VBM_CK(cudaMemsetAsync(ctr + 1, 0, sizeof(uint32_t), st));
     VBM_CK(cudaMemsetAsync(tmask, 0, (size_t)nl * 8u * sizeof(uint64_t), st));
     compact_kernel<<<grid_for(cap, sm), kThreads, 0, st>>>(keys, cap, slot_id, ctr + 1, tkey, tval, pkey);
@@ -377,13 +416,12 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     }
     // 4. Tree order of the leaves; counts, first indices, node ids.
     if (nl) {
-        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, nl, 54, st));
+        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, scan_tmp, nl, 54, st));
         count_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, final_of);
         node_flag_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f);
-        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(cnt, nl, ctr + 5);
-        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(up_f, nl, ctr + 6);
-        devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(lo_f, nl, ctr + 7);
-        VBM_CK(cudaGetLastError());
+        VBM_CK(devsort::scan_exclusive(cnt, nl, ctr + 5, scan_tmp, st));
+        VBM_CK(devsort::scan_exclusive(up_f, nl, ctr + 6, scan_tmp, st));
+        VBM_CK(devsort::scan_exclusive(lo_f, nl, ctr + 7, scan_tmp, st));
     }
     uint32_t tot[3] = {0, 0, 0};
     if (nl) VBM_CK(read_back(tot, ctr + 5, 3, st));
@@ -426,20 +464,7 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     g->max_span = spans[0];
     g->n_over_cache = spans[1];
     set_device_views(g, lay, sm);
-
-    // Host mirrors (vbm_info, vbm_leaf_export).
-    g->leaves.resize(nl);
-    g->root_keys.resize(g->n_upper);
-    g->upper.resize((size_t)g->n_upper * kUpperSlots);
-    g->lower.resize((size_t)g->n_lower * kLowerSlots);
-    g->first_leaf.resize(g->n_blocks);
-    g->jump.resize(g->n_blocks * words);
-    g->nbr.resize((size_t)nl * kNbrStride);
-    void* dst[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
-                    g->first_leaf.data(), g->jump.data(), g->nbr.data()};
-    for (int i = 0; i < 7; ++i)
-        if (lay.bytes[i]) VBM_CK(cudaMemcpyAsync(dst[i], base + lay.off[i], lay.bytes[i], cudaMemcpyDeviceToHost, st));
-    VBM_CK(cudaStreamSynchronize(st));
+    g->mirrors_filled = false;  // host copies are made on the first vbm_leaf_export
 #undef VBM_CK
     return VBM_OK;
 }
@@ -581,7 +606,7 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
         return VBM_ERR_DUPLICATE;
     }
     if (nl) {
-        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, nl, 54, st));
+        VBM_CK(radix_sort(tkey, tval, tkey2, tval2, hist, nullptr, nl, 54, st));
         count_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tval, nl, tmask, cnt, final_of);
         node_flag_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(tkey, nl, up_f, lo_f);
         devsort::scan_exclusive_kernel<<<1, devsort::kScanThreads, 0, st>>>(cnt, nl, ctr + 5);

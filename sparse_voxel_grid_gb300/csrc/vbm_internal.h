@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -93,6 +94,9 @@ struct vbm_grid {
     size_t arena_bytes = 0;
     bool owns_arena = true;    // false: the arena is the caller's (vbm_build_device_noalloc)
     bool host_mirrors = true;  // false: no host copies of the arrays (vbm_build_device_noalloc)
+    // Device-built grids fill the host arrays from the arena on first export.
+    bool mirrors_filled = true;
+    std::mutex mirror_mu;
     int device = -1;
     vbm::DevGrid dev{};
 };

@@ -54,6 +54,91 @@ __global__ void __launch_bounds__(kScanThreads) scan_exclusive_kernel(uint32_t* 
     if (tid == 0 && total) *total = carry_s;
 }
 
+// Multi-CTA exclusive scan, for arrays of many tiles: tile t covers
+// a[t*kScanTile .. (t+1)*kScanTile), one CTA of kScanThreads threads with
+// kScanItems consecutive elements per thread.
+constexpr int kScanItems = 4;
+constexpr uint32_t kScanTile = (uint32_t)kScanThreads * kScanItems;
+
+inline uint32_t scan_tiles(uint64_t n) { return (uint32_t)((n + kScanTile - 1) / kScanTile); }
+
+// Exclusive scan of one value per thread across the CTA; *block_total gets the
+// CTA's sum (all threads).
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sum, uint32_t& block_total) {
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= (uint32_t)d) incl += t;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t ws = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0u;
+        uint32_t wi = ws;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, d);
+            if (lane >= (uint32_t)d) wi += t;
+        }
+        warp_sum[lane] = wi - ws;
+        if (lane == 31) warp_sum[32] = wi;
+    }
+    __syncthreads();
+    block_total = warp_sum[32];
+    return warp_sum[warp] + incl - v;
+}
+
+// sums[t] = sum of tile t.
+__global__ void __launch_bounds__(kScanThreads) tile_sum_kernel(const uint32_t* __restrict__ a, uint64_t n,
+                                                                 uint32_t* __restrict__ sums) {
+    __shared__ uint32_t warp_sum[33];
+    const uint64_t i0 = (uint64_t)blockIdx.x * kScanTile + (uint64_t)threadIdx.x * kScanItems;
+    uint32_t v = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k)
+        if (i0 + k < n) v += a[i0 + k];
+    uint32_t total;
+    block_exclusive_scan(v, warp_sum, total);
+    if (threadIdx.x == 0) sums[blockIdx.x] = total;
+}
+
+// a[i] = offs[t] + the exclusive prefix of a within tile t, in place.
+__global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(uint32_t* __restrict__ a, uint64_t n,
+                                                                  const uint32_t* __restrict__ offs) {
+    __shared__ uint32_t warp_sum[33];
+    const uint64_t i0 = (uint64_t)blockIdx.x * kScanTile + (uint64_t)threadIdx.x * kScanItems;
+    uint32_t v[kScanItems], t = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        v[k] = i0 + k < n ? a[i0 + k] : 0u;
+        t += v[k];
+    }
+    uint32_t total;
+    uint32_t run = offs[blockIdx.x] + block_exclusive_scan(t, warp_sum, total);
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        if (i0 + k < n) a[i0 + k] = run;
+        run += v[k];
+    }
+}
+
+// Exclusive scan of a[0..n) in place, *total (if not NULL) = the sum.  With
+// `tmp` (scan_tiles(n) words of device memory) and more than one tile: per-tile
+// sums, a single-CTA scan of the sums, per-tile scans; otherwise one CTA.
+inline cudaError_t scan_exclusive(uint32_t* a, uint64_t n, uint32_t* total, uint32_t* tmp, cudaStream_t s) {
+    const uint32_t tiles = scan_tiles(n);
+    if (!tmp || tiles <= 1) {
+        scan_exclusive_kernel<<<1, kScanThreads, 0, s>>>(a, n, total);
+        return cudaGetLastError();
+    }
+    tile_sum_kernel<<<tiles, kScanThreads, 0, s>>>(a, n, tmp);
+    scan_exclusive_kernel<<<1, kScanThreads, 0, s>>>(tmp, tiles, total);
+    tile_scan_kernel<<<tiles, kScanThreads, 0, s>>>(a, n, tmp);
+    return cudaGetLastError();
+}
+
 // Per-tile digit histogram: hist[d * n_tiles + tile].
 __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint64_t* __restrict__ keys, uint64_t n,
                                                                    int shift, uint32_t n_tiles,

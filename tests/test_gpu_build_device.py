@@ -58,6 +58,16 @@ def test_workloads_identical(name, log2w):
     del t
 
 
+def test_one_voxel_per_leaf_takes_the_large_table():
+    # 100,000 voxels in 100,000 leaves: more leaves than the first hash table
+    # (sized for one leaf per 16 voxels) holds, so the build retries with the
+    # table of 2n slots
+    c = synth.scatter(side=47, count=100_000, origin=-200, seed=9)
+    assert len(c) == 100_000
+    h, d = _same(c, 7)
+    assert d.info["n_leaves"] == 100_000
+
+
 def test_duplicates_and_dedup():
     t = gu.torch()
     c = np.array([[0, 0, 0], [1, 2, 3], [0, 0, 0], [9, 9, 9], [1, 2, 3]], dtype=np.int32)
