@@ -29,6 +29,10 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute
  *     calls only enqueue work: they return after launching, and launch errors
  *     are reported as VBM_ERR_CUDA.  Results are ready when the stream is.
+ *     They allocate nothing and never synchronise, so they may be captured
+ *     into a CUDA graph, and calls on one grid may run on several streams at
+ *     once.  The builders allocate and synchronise (except
+ *     vbm_build_device_noalloc after its first call on a device).
  *   - Sidecars and filter outputs hold (N+1) rows of C interleaved fp32
  *     channels: row r at [r*C, r*C+C).  Row 0 (background) is never read as a
  *     tap; filters write it as +0.0 so an output can serve as the next sidecar.

@@ -73,6 +73,8 @@ int upload(vbm_grid* g, cudaStream_t stream) {
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);
     vbm::set_device_views(g, lay, sm_count);
+    e = vbm::prepare_device_kernels(g->device);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: kernel attributes", e);
     return VBM_OK;
 }
 

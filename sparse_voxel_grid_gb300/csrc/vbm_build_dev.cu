@@ -21,6 +21,7 @@
 #include <vector>
 
 #include "vbm_internal.h"
+#include "vbm_launch.h"
 #include "vbm_sort.cuh"
 
 namespace vbm {
@@ -464,6 +465,7 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     g->max_span = spans[0];
     g->n_over_cache = spans[1];
     set_device_views(g, lay, sm);
+    VBM_CK(prepare_device_kernels(device));
     g->mirrors_filled = false;  // host copies are made on the first vbm_leaf_export
 #undef VBM_CK
     return VBM_OK;
@@ -662,6 +664,7 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
     g->max_span = spans[0];
     g->n_over_cache = spans[1];
     set_device_views(g, lay, sm);
+    VBM_CK(prepare_device_kernels(device));
 #undef VBM_CK
     return VBM_OK;
 }

@@ -29,6 +29,9 @@ cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, fl
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream);
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream);
 cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream);
+// Per-device kernel attributes (shared-memory opt-ins), set once when a grid
+// is created on the device, outside any stream capture.
+cudaError_t prepare_device_kernels(int device);
 
 // Threads per block for a block width of 2^log2w slots (one slot per thread).
 inline int threads_for(int log2w) { return 1 << log2w; }

@@ -4,6 +4,8 @@
 // Sources (web pages; cited by title and section):
 //   [2258] OpenVDB PR #2258 "VBM select-based inverse-map decode"
 //   [2263] OpenVDB PR #2263 "Alternative stencil resolvers for VoxelBlockManager"
+#include <mutex>
+
 #include "vbm_brick.cuh"
 #include "vbm_launch.h"
 #include "vbm_weno.cuh"
@@ -176,25 +178,28 @@ __global__ void __launch_bounds__(512) brick_weno_kernel(DevGrid g, const float*
 }  // namespace
 
 // Dynamic shared memory above the default 48 KB needs an opt-in per kernel
-// (set on the current device at every launch that needs it).
-template <bool TAPS>
-cudaError_t weno_smem_opt_in(int log2w) {
-    const size_t bytes = weno_smem_bytes(log2w);
-    if (bytes <= 48u * 1024u) return cudaSuccess;
-    return cudaFuncSetAttribute(brick_weno_kernel<TAPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+// and device.  It is set when a grid is created (prepare_device_kernels), so
+// that a launch is nothing but a launch and can be captured into a CUDA graph.
+cudaError_t prepare_device_kernels(int device) {
+    static std::mutex mu;
+    static uint64_t done = 0;  // one bit per device
+    std::lock_guard<std::mutex> lock(mu);
+    if (device >= 0 && device < 64 && ((done >> device) & 1u)) return cudaSuccess;
+    const int bytes = (int)weno_smem_bytes(9);
+    cudaError_t e = cudaFuncSetAttribute(brick_weno_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(brick_weno_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && device >= 0 && device < 64) done |= 1ull << device;
+    return e;
 }
 
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream) {
-    const cudaError_t e = weno_smem_opt_in<false>(g.log2w);
-    if (e != cudaSuccess) return e;
     brick_weno_kernel<false><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, phi, iso, out,
                                                                                                       nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream) {
-    const cudaError_t e = weno_smem_opt_in<true>(g.log2w);
-    if (e != cudaSuccess) return e;
     brick_weno_kernel<true><<<g.n_blocks, threads_for(g.log2w), weno_smem_bytes(g.log2w), stream>>>(g, nullptr, 0.0f,
                                                                                                      nullptr, taps);
     return cudaGetLastError();

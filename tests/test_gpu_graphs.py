@@ -1,0 +1,78 @@
+"""Every compute call only enqueues kernels on the given stream: captured into
+a CUDA graph and replayed, each gives the bits of a direct call, and two
+streams may run calls on one grid at the same time."""
+import numpy as np
+import pytest
+
+import sparse_voxel_grid_gb300 as vbm
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    gu.require_gpu()
+
+
+@pytest.mark.parametrize("log2w", [7, 9])
+def test_graph_capture_and_replay(log2w):
+    t = gu.torch()
+    coords = synth.WORKLOADS["T"]()
+    g = vbm.vbm_build(coords, log2w)
+    n = g.n
+    side = {C: t.from_numpy(synth.sidecar_uniform(n, C, seed=C)).cuda() for C in (1, 3, 16)}
+    direct = {}
+    for C in (1, 3, 16):
+        o = t.empty_like(side[C])
+        vbm.vbm_box_filter(g, side[C], C, o, vbm.RESOLVE_BRICK)
+        direct[("box", C)] = o
+    lap = t.empty_like(side[1])
+    vbm.vbm_cross_filter(g, side[1], 1, lap, vbm.RESOLVE_CACHED, vbm.CROSS_LAPLACIAN)
+    weno = t.empty_like(side[1])
+    vbm.vbm_weno_filter(g, side[1], weno, 0.0, vbm.RESOLVE_BRICK)
+    li = t.empty(g.n_slots, dtype=t.int32, device="cuda")
+    vo = t.empty(g.n_slots, dtype=t.int16, device="cuda")
+    vbm.vbm_decode(g, li, vo)
+    t.cuda.synchronize()
+
+    outs = {C: t.full_like(side[C], float("nan")) for C in (1, 3, 16)}
+    glap, gweno = t.full_like(lap, float("nan")), t.full_like(weno, float("nan"))
+    gli, gvo = t.zeros_like(li), t.zeros_like(vo)
+    s = t.cuda.Stream()
+    graph = t.cuda.CUDAGraph()
+    with t.cuda.stream(s):
+        with t.cuda.graph(graph, stream=s):
+            for C in (1, 3, 16):
+                vbm.vbm_box_filter(g, side[C], C, outs[C], vbm.RESOLVE_BRICK, stream=s)
+            vbm.vbm_cross_filter(g, side[1], 1, glap, vbm.RESOLVE_CACHED, vbm.CROSS_LAPLACIAN, stream=s)
+            vbm.vbm_weno_filter(g, side[1], gweno, 0.0, vbm.RESOLVE_BRICK, stream=s)
+            vbm.vbm_decode(g, gli, gvo, stream=s)
+    for _ in range(2):
+        graph.replay()
+    t.cuda.synchronize()
+    for C in (1, 3, 16):
+        np.testing.assert_array_equal(gu.bits(outs[C].cpu().numpy()), gu.bits(direct[("box", C)].cpu().numpy()))
+    np.testing.assert_array_equal(gu.bits(glap.cpu().numpy()), gu.bits(lap.cpu().numpy()))
+    np.testing.assert_array_equal(gu.bits(gweno.cpu().numpy()), gu.bits(weno.cpu().numpy()))
+    assert t.equal(gli, li) and t.equal(gvo, vo)
+
+
+def test_two_streams_on_one_grid():
+    t = gu.torch()
+    coords = synth.WORKLOADS["S185"]()
+    g = vbm.vbm_build(coords, 9)
+    a = t.from_numpy(synth.sidecar_uniform(g.n, 8, seed=1)).cuda()
+    b = t.from_numpy(synth.sidecar_uniform(g.n, 8, seed=2)).cuda()
+    ra, rb = t.empty_like(a), t.empty_like(b)
+    vbm.vbm_box_filter(g, a, 8, ra, vbm.RESOLVE_BRICK)
+    vbm.vbm_box_filter(g, b, 8, rb, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    s1, s2 = t.cuda.Stream(), t.cuda.Stream()
+    oa, ob = t.full_like(a, float("nan")), t.full_like(b, float("nan"))
+    for _ in range(3):
+        vbm.vbm_box_filter(g, a, 8, oa, vbm.RESOLVE_BRICK, stream=s1)
+        vbm.vbm_box_filter(g, b, 8, ob, vbm.RESOLVE_BRICK, stream=s2)
+    t.cuda.synchronize()
+    assert t.equal(oa.view(t.int32), ra.view(t.int32)) and t.equal(ob.view(t.int32), rb.view(t.int32))
