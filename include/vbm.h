@@ -80,6 +80,9 @@ extern "C" {
 #define VBM_OUTPUT_STREAMED 0     /* each (tap, index) consumed as it is resolved (forEach*) */
 #define VBM_OUTPUT_MATERIALISED 1 /* all taps resolved into a per-thread array first (compute*) */
 
+/* vbm_box_filter_batch: sidecars per call */
+#define VBM_MAX_BATCH 8
+
 /* cross-stencil consumer */
 #define VBM_CROSS_LAPLACIAN 0 /* sum of the active face values (increasing tap order) - 6*centre */
 #define VBM_CROSS_SUM 1       /* sum of the 7 taps' values in tap order */
@@ -220,6 +223,20 @@ int vbm_decode_sweep(const vbm_grid* grid, uint32_t* leaf_index, uint16_t* voxel
  * device arrays of (N+1)*C floats.  Errors: INVALID, STATE, ALIGN, CUDA. */
 int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out, int resolver, int output,
                    void* stream);
+
+/* Several box filters on one grid in one call: out_i = the 27-tap box filter
+ * of sidecars[i] with C[i] channels, for i < count (1..VBM_MAX_BATCH), each
+ * exactly as vbm_box_filter(grid, sidecars[i], C[i], outs[i], resolver,
+ * VBM_OUTPUT_STREAMED, stream) computes it.  With the brick resolver the
+ * filters whose C is 1, 2, 3, 4, 8 or 16 run as one launch whose CTAs
+ * alternate between the sidecars, so that each SM holds CTAs in different
+ * phases (decode and brick build, bound by load latency; gather, bound by the
+ * L1 data pipe); other widths and resolvers launch one filter after another.
+ * sidecars, C and outs are host arrays of `count` entries; no output may alias
+ * a sidecar or another output.  Errors: as vbm_box_filter, INVALID for a bad
+ * count or aliasing. */
+int vbm_box_filter_batch(const vbm_grid* grid, int count, const float* const* sidecars, const int* C,
+                         float* const* outs, int resolver, void* stream);
 
 /* 7-tap cross stencil (centre and the six face neighbours, taps t in
  * {4,10,12,13,14,16,22} of the box numbering) consumed as `op`:

@@ -45,7 +45,7 @@ SENTINEL_OFFSET = 0xFFFF
 
 __all__ = [
     "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
-    "vbm_decode_sweep", "vbm_box_filter", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
+    "vbm_decode_sweep", "vbm_box_filter", "vbm_box_filter_batch", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
     "vbm_weno_taps", "vbm_last_error",
 ]
 
@@ -192,6 +192,24 @@ def vbm_box_filter(grid: Grid, sidecar, C: int, out, resolver: int = RESOLVE_CAC
     check(load().vbm_box_filter(grid.handle, _dev_ptr(sidecar, torch.float32, m, "sidecar"), int(C),
                                 _dev_ptr(out, torch.float32, m, "out"), int(resolver), int(output),
                                 _stream_handle(stream)))
+
+
+def vbm_box_filter_batch(grid: Grid, sidecars, Cs, outs, resolver: int = RESOLVE_BRICK, stream=None) -> None:
+    """Box filters of several (N+1)*C float32 CUDA tensors in one call (see
+    include/vbm.h): outs[i] = box(sidecars[i]) with Cs[i] channels."""
+    import torch
+    k = len(sidecars)
+    if not (len(Cs) == len(outs) == k):
+        raise ValueError("sidecars, Cs and outs must have the same length")
+    sc = (ctypes.c_void_p * max(k, 1))()
+    ou = (ctypes.c_void_p * max(k, 1))()
+    cs = (ctypes.c_int * max(k, 1))()
+    for i in range(k):
+        m = (grid.n + 1) * int(Cs[i])
+        sc[i] = _dev_ptr(sidecars[i], torch.float32, m, "sidecar").value
+        ou[i] = _dev_ptr(outs[i], torch.float32, m, "out").value
+        cs[i] = int(Cs[i])
+    check(load().vbm_box_filter_batch(grid.handle, k, sc, cs, ou, int(resolver), _stream_handle(stream)))
 
 
 def vbm_cross_filter(grid: Grid, sidecar, C: int, out, resolver: int = RESOLVE_CACHED,

@@ -338,6 +338,36 @@ int vbm_box_filter(const vbm_grid* g, const float* sidecar, int C, float* out, i
     return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter: launch", e);
 }
 
+int vbm_box_filter_batch(const vbm_grid* g, int count, const float* const* sidecars, const int* C,
+                         float* const* outs, int resolver, void* stream) {
+    g_last_error.clear();
+    const char* fn = "vbm_box_filter_batch";
+    if (count < 1 || count > VBM_MAX_BATCH) return fail(VBM_ERR_INVALID, std::string(fn) + ": count must be in 1..8");
+    if (!sidecars || !C || !outs) return fail(VBM_ERR_INVALID, std::string(fn) + ": NULL array");
+    for (int i = 0; i < count; ++i) {
+        int rc = check_filter(g, sidecars[i], C[i], outs[i], resolver, fn);
+        if (rc) return rc;
+        for (int j = 0; j < count; ++j) {
+            if (j != i && (const void*)outs[i] == (const void*)sidecars[j])
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": an output aliases a sidecar");
+            if (j < i && outs[i] == outs[j]) return fail(VBM_ERR_INVALID, std::string(fn) + ": two outputs alias");
+        }
+    }
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (g->n_blocks == 0) {
+        for (int i = 0; i < count && e == cudaSuccess; ++i) e = cudaMemsetAsync(outs[i], 0, sizeof(float) * (size_t)C[i], s);
+    } else if (resolver == VBM_RESOLVE_BRICK) {
+        e = vbm::launch_brick_box_batch(g->dev, count, sidecars, C, outs, s);
+    } else {
+        for (int i = 0; i < count && e == cudaSuccess; ++i)
+            e = vbm::launch_box_filter(g->dev, sidecars[i], C[i], outs[i], resolver, VBM_OUTPUT_STREAMED, s);
+    }
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter_batch: launch", e);
+}
+
 int vbm_cross_filter(const vbm_grid* g, const float* sidecar, int C, float* out, int resolver, int op,
                      void* stream) {
     g_last_error.clear();

@@ -222,16 +222,16 @@ __device__ __forceinline__ BrickSmem carve(unsigned char* smem, int log2w) {
     return m;
 }
 
-// Filter kernel: channels [ch_begin, ch_begin + lanes*CC); `lanes` threads per
-// voxel, each handling CC consecutive channels (VEC: as float4s).  VALUES: one
-// channel, value bricks (lanes == CC == 1).
+// The filter of VBM block b: channels [ch_begin, ch_begin + lanes*CC);
+// `lanes` threads per voxel, each handling CC consecutive channels (VEC: as
+// float4s).  VALUES: one channel, value bricks (lanes == CC == 1).
 template <int KIND, int CC, bool VEC, bool VALUES, int CT>
-__global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
-                                                           float* __restrict__ out, int C, int ch_begin, int lanes) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__device__ __forceinline__ void brick_filter_block(const DevGrid& g, uint32_t b, const float* __restrict__ sc,
+                                                   float* __restrict__ out, int C, int ch_begin, int lanes,
+                                                   unsigned char* smem) {
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
-    brick_prologue<!VEC>(g, k, m.offs, m.lof, m.starts);
+    brick_prologue<!VEC>(g, k, m.offs, m.lof, m.starts, b);
     const uint32_t L = CT > 0 ? (uint32_t)(CT / CC) : (uint32_t)lanes;
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
@@ -253,7 +253,47 @@ __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const floa
         }
         __syncthreads();  // the next round overwrites the bricks
     }
-    if (blockIdx.x == 0 && threadIdx.x < L * CC) out[ch_begin + threadIdx.x] = 0.0f;
+    if (b == 0 && threadIdx.x < L * CC) out[ch_begin + threadIdx.x] = 0.0f;
+}
+
+template <int KIND, int CC, bool VEC, bool VALUES, int CT>
+__global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
+                                                           float* __restrict__ out, int C, int ch_begin, int lanes) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    brick_filter_block<KIND, CC, VEC, VALUES, CT>(g, blockIdx.x, sc, out, C, ch_begin, lanes, smem);
+}
+
+// Several box filters in one launch: CTA i filters block i / count of sidecar
+// i % count, so the CTAs resident on an SM belong to different sidecars and
+// are in different phases (decode and brick build, bound by load latency;
+// gather, bound by the L1 data pipe) rather than all in the same one.  Channel
+// counts with a compile-time layout only (kBatchWidths).
+constexpr int kMaxBatch = VBM_MAX_BATCH;  // include/vbm.h
+struct BoxBatch {
+    const float* sc[kMaxBatch];
+    float* out[kMaxBatch];
+    int C[kMaxBatch];
+    int count;
+};
+
+__host__ __device__ constexpr bool batch_width(int C) {
+    return C == 1 || C == 2 || C == 3 || C == 4 || C == 8 || C == 16;
+}
+
+__global__ void __launch_bounds__(512, 4) brick_box_batch_kernel(DevGrid g, BoxBatch a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const uint32_t e = blockIdx.x % (uint32_t)a.count, b = blockIdx.x / (uint32_t)a.count;
+    const float* sc = a.sc[e];
+    float* out = a.out[e];
+    switch (a.C[e]) {  // uniform per CTA
+        case 1: brick_filter_block<0, 1, false, true, 1>(g, b, sc, out, 1, 0, 1, smem); break;
+        case 2: brick_filter_block<0, 2, false, false, 2>(g, b, sc, out, 2, 0, 1, smem); break;
+        case 3: brick_filter_block<0, 3, false, false, 3>(g, b, sc, out, 3, 0, 1, smem); break;
+        case 4: brick_filter_block<0, 4, true, false, 4>(g, b, sc, out, 4, 0, 1, smem); break;
+        case 8: brick_filter_block<0, 4, true, false, 8>(g, b, sc, out, 8, 0, 2, smem); break;
+        case 16: brick_filter_block<0, 4, true, false, 16>(g, b, sc, out, 16, 0, 4, smem); break;
+        default: break;
+    }
 }
 
 // Raw taps through the index bricks.  SHAPE 27 (box) or 7 (cross).
@@ -262,7 +302,7 @@ __global__ void __launch_bounds__(512) brick_taps_kernel(DevGrid g, uint32_t* __
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
-    brick_prologue<true>(g, k, m.offs, m.lof, m.starts);
+    brick_prologue<true>(g, k, m.offs, m.lof, m.starts, blockIdx.x);
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
@@ -315,6 +355,28 @@ cudaError_t launch_brick_kind(const DevGrid& g, const float* sc, int C, float* o
 
 cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, float* out, cudaStream_t stream) {
     return launch_brick_kind<0>(g, sidecar, C, out, stream);
+}
+
+cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* const* sidecars, const int* C,
+                                   float* const* outs, cudaStream_t stream) {
+    BoxBatch a{};
+    a.count = 0;
+    for (int i = 0; i < count; ++i) {
+        if (batch_width(C[i])) {  // fused
+            a.sc[a.count] = sidecars[i];
+            a.out[a.count] = outs[i];
+            a.C[a.count] = C[i];
+            ++a.count;
+        } else {
+            const cudaError_t e = launch_brick_kind<0>(g, sidecars[i], C[i], outs[i], stream);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    if (a.count == 0) return cudaSuccess;
+    const uint64_t ctas = (uint64_t)g.n_blocks * (uint64_t)a.count;
+    if (ctas > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+    brick_box_batch_kernel<<<(unsigned)ctas, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(g, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream) {

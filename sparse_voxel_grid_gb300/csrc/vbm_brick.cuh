@@ -21,14 +21,14 @@ struct BrickCtx {
     const uint64_t* jb;
 };
 
-// Decode every valid slot of the block (select-based decode, [2258] "What
+// Decode every valid slot of VBM block b (select-based decode, [2258] "What
 // changed") into offs/lof and record where each spanned leaf starts.  Ends with
 // a barrier.
 __device__ __forceinline__ void brick_prologue_direct(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
+                                               uint16_t* starts, uint32_t b) {
     k.W = 1u << g.log2w;
     const uint32_t words = k.W >> 6;
-    k.b = blockIdx.x;
+    k.b = b;
     k.jb = g.jump + (size_t)k.b * words;
     k.fl = __ldg(&g.first_leaf[k.b]);
     k.span = block_span(k.jb, words);
@@ -44,13 +44,13 @@ __device__ __forceinline__ void brick_prologue_direct(const DevGrid& g, BrickCtx
 }
 
 __device__ __forceinline__ void brick_prologue_staged(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
+                                               uint16_t* starts, uint32_t b) {
     // The block's jumpMap words and their popcount prefixes, staged once.
     __shared__ uint64_t s_jw[8];
     __shared__ uint32_t s_cum[9];
     k.W = 1u << g.log2w;
     const uint32_t words = k.W >> 6;
-    k.b = blockIdx.x;
+    k.b = b;
     k.jb = g.jump + (size_t)k.b * words;
     k.fl = __ldg(&g.first_leaf[k.b]);
     k.n_valid = min(k.W, g.n - k.b * k.W);
@@ -91,9 +91,9 @@ __device__ __forceinline__ void brick_prologue_staged(const DevGrid& g, BrickCtx
 // (measured faster for the float4-lane layouts).
 template <bool STAGED>
 __device__ __forceinline__ void brick_prologue(const DevGrid& g, BrickCtx& k, uint16_t* offs, uint16_t* lof,
-                                               uint16_t* starts) {
-    if constexpr (STAGED) brick_prologue_staged(g, k, offs, lof, starts);
-    else brick_prologue_direct(g, k, offs, lof, starts);
+                                               uint16_t* starts, uint32_t b) {
+    if constexpr (STAGED) brick_prologue_staged(g, k, offs, lof, starts, b);
+    else brick_prologue_direct(g, k, offs, lof, starts, b);
 }
 
 }  // namespace brick

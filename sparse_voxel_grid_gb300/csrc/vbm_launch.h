@@ -25,6 +25,10 @@ cudaError_t launch_weno_taps(const DevGrid& g, uint32_t* taps, int resolver, cud
 
 // Brick resolver (vbm_brick.cu).
 cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, float* out, cudaStream_t stream);
+// count (1..VBM_MAX_BATCH) box filters; the widths with a compile-time layout
+// share one launch, the others are launched one by one.
+cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* const* sidecars, const int* C,
+                                   float* const* outs, cudaStream_t stream);
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream);
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream);
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream);

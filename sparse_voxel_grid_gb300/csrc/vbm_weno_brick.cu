@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(512) brick_weno_kernel(DevGrid g, const float*
     extern __shared__ __align__(16) unsigned char smem[];
     const WenoSmem m = carve_weno(smem, g.log2w);
     BrickCtx k;
-    brick_prologue<true>(g, k, m.offs, m.lof, m.starts);
+    brick_prologue<true>(g, k, m.offs, m.lof, m.starts, blockIdx.x);
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
         weno_build_round<!TAPS>(g, k, m.offs, m.starts, l0, nb, m.wb, phi);

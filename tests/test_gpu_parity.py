@@ -188,6 +188,40 @@ def test_box_16_byte_aligned_buffers(C):
         np.testing.assert_array_equal(gu.bits(obuf[shift:shift + m].cpu().numpy()), want)
 
 
+@pytest.mark.parametrize("widths", [(1, 3, 8, 16), (16, 1), (5, 2, 13, 4), (8,)])
+@pytest.mark.parametrize("resolver", RESOLVERS)
+def test_box_filter_batch(case, widths, resolver):
+    # one call filtering several sidecars equals separate calls, bit for bit;
+    # with the brick resolver the widths 1/2/3/4/8/16 share one launch
+    t = gu.torch()
+    _, coords, o = case
+    for log2w in (6, 9):
+        g = vbm.vbm_build(coords, log2w)
+        sides = [gu.to_dev(synth.sidecar_uniform(o.n, C, seed=10 + i)) for i, C in enumerate(widths)]
+        outs = [t.full_like(s, float("nan")) for s in sides]
+        vbm.vbm_box_filter_batch(g, sides, list(widths), outs, resolver)
+        t.cuda.synchronize()
+        for s, C, out in zip(sides, widths, outs):
+            want = gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
+            np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C} W=2^{log2w}")
+
+
+def test_box_filter_batch_errors():
+    t = gu.torch()
+    g = vbm.vbm_build(SMALL["tiny_shell"](), 7)
+    s = t.zeros(g.n + 1, device="cuda")
+    o = t.zeros(g.n + 1, device="cuda")
+    with pytest.raises(vbm.VbmError):
+        vbm.vbm_box_filter_batch(g, [], [], [])
+    with pytest.raises(vbm.VbmError):
+        vbm.vbm_box_filter_batch(g, [s] * 9, [1] * 9, [o] * 9)
+    with pytest.raises(vbm.VbmError):  # two outputs alias
+        vbm.vbm_box_filter_batch(g, [s, s], [1, 1], [o, o])
+    s2 = t.zeros(g.n + 1, device="cuda")
+    with pytest.raises(vbm.VbmError):  # an output is another entry's sidecar
+        vbm.vbm_box_filter_batch(g, [s, s2], [1, 1], [s2, o])
+
+
 def test_empty_grid():
     t = gu.torch()
     g = vbm.vbm_build(np.zeros((0, 3), dtype=np.int32), 7)
