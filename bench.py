@@ -3,17 +3,20 @@
 Workload: the sphere shell of radius 185 and thickness 3 (183.5 <= |p| <= 186.5,
 1,290,538 active voxels in 11,255 leaves), fp32 sidecars U[-1,1) with C
 interleaved channels.  One step = the 27-tap box filter (select-based decode +
-brick resolver + streamed gather/accumulate, one fused kernel) over every
-active voxel at C = 1, 3, 8 and 16, BlockWidth 512: four launches.  `value`
-counts each voxel once per channel width: 4 * N voxels per step.  The other
-resolvers (the pages' tree walk and cached table), both output modes, both
-block widths, the cross Laplacian and the decode are timed in `variants`.
+brick resolver + streamed gather/accumulate, fused) over every active voxel of
+four sidecars, C = 1, 3, 8 and 16, BlockWidth 512, in one
+vbm_box_filter_batch call: one launch whose CTAs alternate between the four
+sidecars (`--step separate`: four calls).  `value` counts each voxel once per
+sidecar: 4 * N voxels per step.  Each width is also timed alone (`detail`);
+the other resolvers (the pages' tree walk and cached table), both output
+modes, both block widths, the cross Laplacian, the WENO consumer, the decodes
+and the builders are timed in `variants`.
 
-Timing: each launch is bracketed by CUDA events on the launching stream; L2 is
-flushed (a write of twice its size) before every launch, outside the events.
-The step time is the sum of its four launch times.  A JSON line is printed on
-rank 0.  `--impl reference` times the CPU oracle on the host cores instead,
-on a bounded sample of the same workload.
+Timing: each step (and each detail launch) is bracketed by CUDA events on the
+launching stream; L2 is flushed (a write of twice its size) before each,
+outside the events.  A JSON line is printed on rank 0.  `--impl reference`
+times the CPU oracle on the host cores instead, on a bounded sample of the
+same workload.
 """
 from __future__ import annotations
 
@@ -167,6 +170,13 @@ def run_gpu(args):
     def launch(C, output=vbm.OUTPUT_STREAMED, grid=g):
         vbm.vbm_box_filter(grid, sidecars[C], C, outs[C], resolver, output, stream)
 
+    def launch_step():
+        if args.step == "batch":  # all widths in one call (one launch with the brick resolver)
+            vbm.vbm_box_filter_batch(g, [sidecars[C] for C in CS], list(CS), [outs[C] for C in CS], resolver, stream)
+        else:
+            for C in CS:
+                launch(C)
+
     def timed_launch(fn):
         flush_buf.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -178,30 +188,32 @@ def run_gpu(args):
 
     # warm-up
     for _ in range(args.warmup):
+        timed_launch(launch_step)
         for C in CS:
             timed_launch(lambda C=C: launch(C))
     torch.cuda.synchronize()
 
-    # timed region
+    # timed region: K steps, L2 flushed before each (outside the events)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t0 = time.perf_counter()
-        evs = {C: [] for C in CS}
-        for _ in range(args.steps):
-            for C in CS:
-                evs[C].append(timed_launch(lambda C=C: launch(C)))
+        step_evs = [timed_launch(launch_step) for _ in range(args.steps)]
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         wall = time.perf_counter() - t0
-    per_c_ms = {C: [a.elapsed_time(b) for a, b in evs[C]] for C in CS}
-    step_ms = [sum(per_c_ms[C][k] for C in CS) for k in range(args.steps)]
+    step_ms = [a.elapsed_time(b) for a, b in step_evs]
     ms_per_step = statistics.mean(step_ms)
     if dist:
         ms_per_step = max_over_ranks(ms_per_step, device="cuda")
     value = world * len(CS) * n / (ms_per_step * 1e-3)
+
+    # per-width detail: each width alone, K launches, L2 flushed before each
+    evs = {C: [timed_launch(lambda C=C: launch(C)) for _ in range(args.steps)] for C in CS}
+    torch.cuda.synchronize()
+    per_c_ms = {C: [a.elapsed_time(b) for a, b in evs[C]] for C in CS}
 
     peak_gbs, peak_kind = peaks()
     detail = {}
@@ -212,11 +224,18 @@ def run_gpu(args):
                            "ms_min": round(min(per_c_ms[C]), 5), "voxels_per_s": n / (ms * 1e-3),
                            "alg_bytes": b, "gbs": b / (ms * 1e-3) / 1e9,
                            "frac_of_hbm": b / (ms * 1e-3) / 1e9 / peak_gbs}
-    dom = max(CS, key=lambda C: statistics.mean(per_c_ms[C]))
-    dom_ms = statistics.mean(per_c_ms[dom])
-    dom_bytes = algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, dom)
+    if args.step == "batch":  # the step's kernel is the batched launch
+        dom_label = f"box filter batch ({args.resolver} resolver, C=1,3,8,16 in one call)"
+        dom_ms = ms_per_step
+        dom_bytes = sum(algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, C) for C in CS)
+        traffic = load_traffic(f"box_{args.resolver}_batch_W{W}")
+    else:
+        dom = max(CS, key=lambda C: statistics.mean(per_c_ms[C]))
+        dom_label = f"box filter ({args.resolver} resolver, streamed) C={dom}"
+        dom_ms = statistics.mean(per_c_ms[dom])
+        dom_bytes = algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, dom)
+        traffic = load_traffic(f"box_{args.resolver}_W{W}_C{dom}")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = load_traffic(f"box_{args.resolver}_W{W}_C{dom}")
 
     # end to end through the public API: pinned host sidecar -> device -> filter -> host
     e2e = None
@@ -236,13 +255,13 @@ def run_gpu(args):
         "config": workload_config(args, n, info["n_leaves"], info["n_blocks"], info["n_blocks_over_cache"],
                                   info["max_span"], world),
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
-        "roofline": {"bound": "hbm", "kernel": f"box filter ({args.resolver} resolver, streamed) C={dom}", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": dom_label, "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes},
         "detail": detail,
         "e2e": e2e,
-        "gpu_launches": len(CS) * args.steps,
+        "gpu_launches": (1 if args.step == "batch" and args.resolver == "brick" else len(CS)) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "variants": variants,
@@ -257,7 +276,9 @@ def workload_config(args, n, n_leaves, n_blocks, n_over, max_span, world):
     """The `config` object both arms print for the same workload."""
     W = 1 << args.log2w
     return {"workload": f"{WORKLOADS[args.workload]}, N={n}, leaves={n_leaves}, fused decode + {args.resolver} "
-                        f"resolver + streamed 27-tap box filter at C=1,3,8,16 (4 launches per step), W={W}",
+                        f"resolver + streamed 27-tap box filter at C=1,3,8,16, W={W}",
+            "step": "one vbm_box_filter_batch call (one launch with the brick resolver)" if args.step == "batch"
+                    else "four vbm_box_filter calls",
             "n_active": n, "n_leaves": n_leaves, "block_width": W, "channels": list(CS), "n_blocks": n_blocks,
             "n_blocks_over_cache": n_over, "max_span": max_span, "resolver": args.resolver, "output": "streamed",
             "l2": "flushed before every launch", "value_counts": "4*N voxels per step (one per channel width)",
@@ -556,6 +577,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", choices=["batch", "separate"], default="batch",
+                    help="the four widths in one vbm_box_filter_batch call (default) or four calls")
     ap.add_argument("--decode-ab", action="store_true",
                     help="time the select decode against the sweep decode and print that table instead")
     args = ap.parse_args()

@@ -28,7 +28,7 @@ def test_cpu_baseline_on_two_processes():
 
 def test_workload_config_is_shared_by_both_arms():
     class A:
-        log2w, workload, resolver = 9, "S185", "brick"
+        log2w, workload, resolver, step = 9, "S185", "brick", "batch"
     c = bench.workload_config(A, 1290538, 11255, 2521, 0, 13, 1)
     assert c["block_width"] == 512 and c["n_blocks"] == 2521 and c["channels"] == [1, 3, 8, 16]
     assert c["workload"].startswith(bench.WORKLOADS["S185"])
