@@ -13,32 +13,48 @@
 //   - the CTA stages the firstLeafID and jumpMap words of the blocks its range
 //     overlaps in shared memory, with per-word popcount prefixes, so the rank
 //     is a shared-memory lookup plus one popcount;
-//   - each thread decodes up to kMaxPerThread slots in explicit stages (all
-//     leaf-record loads, then all mask-word loads, then the selects), so its
-//     chains overlap instead of running one after another;
+//   - each thread decodes pairs of consecutive slots (a, a+1), a even, in
+//     explicit stages (all leaf-record loads, then all mask-word loads, then
+//     the selects), so its chains overlap instead of running one after
+//     another, and stores each pair with one 8-byte and one 4-byte store;
+//   - slot a ranks and selects; slot a+1 holds the next active voxel, so its
+//     offset is the next set bit of the same mask word (one find-first-set;
+//     rarely a later word), or the first set bit of the next leaf when one
+//     starts there: the select of rank r+1 taken one step from rank r
+//     (decode on the 20.4M-slot grid D: 134 -> 107 us);
 //   - the word search reads the leaf's directory in its pre-added form, the
 //     eight 32-bit per-word base indices (first index + set bits in the words
 //     before), two 128-bit loads and seven 32-bit compares against the slot's
 //     index, instead of unpacking seven 9-bit fields of a 64-bit word.  The
 //     same comparisons, so the same word and rank; fewer instructions (decode
-//     on the 20.4M-slot grid D: 146 -> 134 us).
+//     on D: 146 -> 134 us).
 #include "vbm_device.cuh"
 #include "vbm_launch.h"
 
 namespace vbm {
 namespace {
 
-#ifndef VBM_DECODE_PER_THREAD
-#define VBM_DECODE_PER_THREAD 2
+#ifndef VBM_DECODE_PAIRS
+#define VBM_DECODE_PAIRS 2
 #endif
 #ifndef VBM_DECODE_MIN_CTAS
 #define VBM_DECODE_MIN_CTAS 16
 #endif
 constexpr int kDecodeThreads = 128;
-constexpr int kMaxPerThread = VBM_DECODE_PER_THREAD;        // slots per thread at most
-constexpr int kMaxRange = kDecodeThreads * kMaxPerThread;   // slots per chunk
+constexpr int kPairs = VBM_DECODE_PAIRS;                    // slot pairs per thread per chunk
+constexpr int kMaxRange = kDecodeThreads * 2 * kPairs;      // slots per chunk
 constexpr int kMaxBlocks = kMaxRange / 64 + 2;              // blocks a chunk can overlap
 constexpr int kMaxWords = 8;                                // jumpMap words per block (W = 512)
+
+// Position of the first set bit of leaf L's mask at word w or later (the leaf
+// has one there).
+__device__ __forceinline__ uint32_t first_bit_from(const LeafRec* __restrict__ rec, uint32_t w) {
+    for (; w < 7u; ++w) {
+        const uint64_t m = __ldg(&rec->mask[w]);
+        if (m) return 64u * w + (uint32_t)__ffsll((long long)m) - 1u;
+    }
+    return 64u * 7u + (uint32_t)__ffsll((long long)__ldg(&rec->mask[7])) - 1u;
+}
 
 __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_kernel(DevGrid g, uint32_t n_cta, uint32_t* __restrict__ leaf_index,
                                                                 uint16_t* __restrict__ voxel_offset) {
@@ -48,9 +64,10 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
 
     const uint32_t log2w = (uint32_t)g.log2w, W = 1u << log2w, words = W >> 6;
     const uint64_t n_slots = (uint64_t)g.n_blocks << log2w;
-    const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta), r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta);
-    // The CTA's range [r0, r1) in chunks of at most kMaxRange slots (uniform per CTA).
-    for (uint32_t s0 = r0; s0 < r1; s0 += kMaxRange) {
+    // The CTA's range [r0, r1), even-aligned so that slot pairs start on even slots.
+    const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta) & ~1u;
+    const uint32_t r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta) & ~1u;
+    for (uint32_t s0 = r0; s0 < r1; s0 += kMaxRange) {  // uniform per CTA
         const uint32_t s1 = min(r1, s0 + (uint32_t)kMaxRange);
         const uint32_t b0 = s0 >> log2w, nb = ((s1 - 1u) >> log2w) - b0 + 1u;
 
@@ -69,32 +86,35 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             }
         }
         __syncthreads();
+        auto rank_leaf = [&](uint32_t slot) {  // leaf of a slot: firstLeafID + jumpMap rank
+            const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
+            const uint64_t keep = (2ull << (s & 63u)) - 1ull;
+            return s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(s_jw[bl][ws] & keep);
+        };
 
-        // Stage 2: rank -> leaf; load every slot's per-word bases (the 9-bit
-        // directory pre-added to the leaf's first index).
-        uint32_t leaf[kMaxPerThread];
-        uint4 blo[kMaxPerThread], bhi[kMaxPerThread];
+        // Each thread decodes pairs of slots (a, a+1), a even.  The first by
+        // rank + select; the second is the next voxel: the next set bit of the
+        // same leaf, or the first set bit of the next leaf when one starts there.
+        uint32_t la[kPairs], lb[kPairs];
+        uint4 blo[kPairs], bhi[kPairs];
 #pragma unroll
-        for (int k = 0; k < kMaxPerThread; ++k) {
-            const uint32_t slot = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads;
-            leaf[k] = kNone;
-            if (slot < s1 && slot < g.n) {  // index = slot + 1 <= N
-                const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
-                const uint64_t keep = (2ull << (s & 63u)) - 1ull;
-                leaf[k] = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(s_jw[bl][ws] & keep);
-                const uint4* base = reinterpret_cast<const uint4*>(g.leaves[leaf[k]].base);
+        for (int k = 0; k < kPairs; ++k) {
+            const uint32_t a = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads);
+            la[k] = lb[k] = kNone;
+            if (a < s1 && a < g.n) {  // index = a + 1 <= N
+                la[k] = rank_leaf(a);
+                if (a + 1u < g.n) lb[k] = rank_leaf(a + 1u);
+                const uint4* base = reinterpret_cast<const uint4*>(g.leaves[la[k]].base);
                 blo[k] = __ldg(base);
                 bhi[k] = __ldg(base + 1);
             }
         }
-        // Stage 3: word of the slot's voxel = bases w = 1..7 at or below its
-        // index; the rank within the word; load the mask words.
-        uint64_t word[kMaxPerThread];
-        uint32_t wsel[kMaxPerThread], r[kMaxPerThread];
+        uint64_t word[kPairs];
+        uint32_t wsel[kPairs], r[kPairs];
 #pragma unroll
-        for (int k = 0; k < kMaxPerThread; ++k) {
-            if (leaf[k] == kNone) continue;
-            const uint32_t index = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads + 1u;
+        for (int k = 0; k < kPairs; ++k) {
+            if (la[k] == kNone) continue;
+            const uint32_t index = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads) + 1u;
             const uint32_t b[8] = {blo[k].x, blo[k].y, blo[k].z, blo[k].w, bhi[k].x, bhi[k].y, bhi[k].z, bhi[k].w};
             uint32_t w = 0, before = b[0];
 #pragma unroll
@@ -105,20 +125,26 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             }
             wsel[k] = w;
             r[k] = index - before;
-            word[k] = __ldg(&g.leaves[leaf[k]].mask[w]);
+            word[k] = __ldg(&g.leaves[la[k]].mask[w]);
         }
-        // Stage 4: in-word select and coalesced stores (sentinels past N).
 #pragma unroll
-        for (int k = 0; k < kMaxPerThread; ++k) {
-            const uint32_t slot = s0 + threadIdx.x + (uint32_t)k * kDecodeThreads;
-            if (slot >= s1) continue;
-            if (leaf[k] == kNone) {
-                leaf_index[slot] = kNone;
-                voxel_offset[slot] = kNoOffset;
-            } else {
-                leaf_index[slot] = leaf[k];
-                voxel_offset[slot] = (uint16_t)(64u * wsel[k] + select64(word[k], r[k]));
+        for (int k = 0; k < kPairs; ++k) {
+            const uint32_t a = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads);
+            if (a >= s1) continue;
+            uint32_t oa = kNoOffset, ob = kNoOffset;
+            if (la[k] != kNone) {
+                const uint32_t bit = select64(word[k], r[k]);
+                oa = 64u * wsel[k] + bit;
+                if (lb[k] == la[k]) {  // the next set bit of the same leaf
+                    const uint64_t rest = bit == 63u ? 0ull : word[k] & (~0ull << (bit + 1u));
+                    ob = rest ? 64u * wsel[k] + (uint32_t)__ffsll((long long)rest) - 1u
+                              : first_bit_from(g.leaves + la[k], wsel[k] + 1u);
+                } else if (lb[k] != kNone) {  // a leaf starts at slot a+1
+                    ob = first_bit_from(g.leaves + lb[k], 0u);
+                }
             }
+            reinterpret_cast<uint2*>(leaf_index)[a >> 1] = make_uint2(la[k], lb[k]);
+            reinterpret_cast<ushort2*>(voxel_offset)[a >> 1] = make_ushort2((uint16_t)oa, (uint16_t)ob);
         }
         __syncthreads();  // the next chunk overwrites the staged metadata
     }
