@@ -36,6 +36,7 @@ def test_graph_capture_and_replay(log2w):
     vo = t.empty(g.n_slots, dtype=t.int16, device="cuda")
     vbm.vbm_decode(g, li, vo)
     t.cuda.synchronize()
+    bouts = {C: t.full_like(side[C], float("nan")) for C in (1, 3, 16)}
 
     outs = {C: t.full_like(side[C], float("nan")) for C in (1, 3, 16)}
     glap, gweno = t.full_like(lap, float("nan")), t.full_like(weno, float("nan"))
@@ -49,6 +50,8 @@ def test_graph_capture_and_replay(log2w):
             vbm.vbm_cross_filter(g, side[1], 1, glap, vbm.RESOLVE_CACHED, vbm.CROSS_LAPLACIAN, stream=s)
             vbm.vbm_weno_filter(g, side[1], gweno, 0.0, vbm.RESOLVE_BRICK, stream=s)
             vbm.vbm_decode(g, gli, gvo, stream=s)
+            vbm.vbm_box_filter_batch(g, [side[C] for C in (1, 3, 16)], [1, 3, 16], [bouts[C] for C in (1, 3, 16)],
+                                     vbm.RESOLVE_BRICK, stream=s)
     for _ in range(2):
         graph.replay()
     t.cuda.synchronize()
@@ -57,6 +60,8 @@ def test_graph_capture_and_replay(log2w):
     np.testing.assert_array_equal(gu.bits(glap.cpu().numpy()), gu.bits(lap.cpu().numpy()))
     np.testing.assert_array_equal(gu.bits(gweno.cpu().numpy()), gu.bits(weno.cpu().numpy()))
     assert t.equal(gli, li) and t.equal(gvo, vo)
+    for C in (1, 3, 16):
+        np.testing.assert_array_equal(gu.bits(bouts[C].cpu().numpy()), gu.bits(direct[("box", C)].cpu().numpy()))
 
 
 def test_two_streams_on_one_grid():
