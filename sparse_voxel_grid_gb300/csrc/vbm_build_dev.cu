@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -277,16 +278,49 @@ __global__ void span_kernel(const unsigned long long* __restrict__ jump, uint32_
 
 namespace {
 
-// Device allocations freed on scope exit.
+// The builder's scratch memory comes from a stream-ordered pool of its own,
+// one per device, which keeps up to kPoolKeep bytes between builds: a build
+// after the first allocates and frees without cudaMalloc / cudaFree (which
+// synchronise the device).  The grid's own arena is a plain cudaMalloc.
+constexpr uint64_t kPoolKeep = 2ull << 30;
+
+cudaError_t scratch_pool(int device, cudaMemPool_t* out) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[device]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t p;
+        cudaError_t e = cudaMemPoolCreate(&p, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = kPoolKeep;
+        e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return e;
+        }
+        pools[device] = p;
+    }
+    *out = pools[device];
+    return cudaSuccess;
+}
+
+// Device allocations from the pool, freed (stream-ordered) on scope exit.
 struct Scratch {
+    cudaMemPool_t pool = nullptr;
+    cudaStream_t stream = nullptr;
     std::vector<void*> ptrs;
     ~Scratch() {
-        for (void* p : ptrs) cudaFree(p);
+        for (void* p : ptrs) cudaFreeAsync(p, stream);
     }
     template <typename T>
     cudaError_t alloc(T** p, size_t count) {
         void* q = nullptr;
-        const cudaError_t e = cudaMalloc(&q, count ? count * sizeof(T) : sizeof(T));
+        const cudaError_t e = cudaMallocFromPoolAsync(&q, count ? count * sizeof(T) : sizeof(T), pool, stream);
         if (e == cudaSuccess) ptrs.push_back(q);
         *p = static_cast<T*>(q);
         return e;
@@ -348,6 +382,8 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
     VBM_CK(cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device));
     const uint32_t W = 1u << log2w, words = W >> 6;
     Scratch sc;
+    sc.stream = st;
+    VBM_CK(scratch_pool(device, &sc.pool));
 
     // 1-2. Leaf hash table and compaction.  The table is first sized for one
     // leaf per 16 voxels (power of two, at most half full); a grid with more
