@@ -135,12 +135,14 @@ int vbm_build(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t 
  * into tree order, scans for first indices and node ids, parallel fill of the
  * leaf records, child tables, VBM block metadata and neighbour rows); the
  * result equals vbm_build's array for array.  Temporary device memory is
- * allocated and freed inside the call (about 12 bytes per voxel for the hash
- * table plus ~150 bytes per leaf), from a stream-ordered pool of the library's
- * own per device that keeps up to 2 GB between builds (the first build on a
- * device creates it); the call synchronises `stream`.  The grid
- * lives on the device only; the first vbm_leaf_export copies its arrays to the
- * host (synchronously, once per grid).  Requires
+ * allocated and freed inside the call: a leaf hash table of 12 bytes per slot,
+ * first sized for one leaf per 16 voxels (about 1.5 bytes per voxel) and
+ * rebuilt at 2n slots if the grid has more leaves, plus ~150 bytes per leaf.
+ * It comes from a stream-ordered pool of the library's own per device that
+ * keeps up to 2 GB between builds (the first build on a device creates it).
+ * The call synchronises `stream`.  The grid lives on the device only; the
+ * first vbm_leaf_export copies its arrays to the host (synchronously, once per
+ * grid).  Requires
  * |x|,|y|,|z| < 2^20 (VBM_ERR_RANGE otherwise).  Errors: as vbm_build. */
 int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* stream,
                      vbm_grid** out);
