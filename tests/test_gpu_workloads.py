@@ -82,6 +82,20 @@ def test_shell_box_filter(shell, C, log2w):
     assert (ref[:C] == 0).all()
 
 
+def test_shell_box_filter_batch(shell):
+    # the benchmarked call: four sidecars in one launch, bit for bit as four calls
+    coords, o = shell
+    t = gu.torch()
+    g = vbm.vbm_build(coords, 9)
+    sides = [gu.to_dev(synth.sidecar_uniform(o.n, C, seed=0)) for C in (1, 3, 8, 16)]
+    outs = [t.full_like(s, float("nan")) for s in sides]
+    vbm.vbm_box_filter_batch(g, sides, [1, 3, 8, 16], outs, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    for s, C, out in zip(sides, (1, 3, 8, 16), outs):
+        want = gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_BRICK, vbm.OUTPUT_STREAMED))
+        np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C}")
+
+
 def test_shell_laplacian(shell):
     coords, o = shell
     s = synth.sidecar_uniform(o.n, 1, seed=0)
@@ -156,6 +170,19 @@ def test_fog_box_filter():
     which = _sample(o.n, k=6000)
     want = gu.bits(o.box_filter(s, C, which=which)).reshape(-1, C)
     np.testing.assert_array_equal(cached.reshape(-1, C)[which], want)
+
+
+def test_fog_box_filter_batch():
+    coords = synth.WORKLOADS["F"]()
+    t = gu.torch()
+    g = vbm.vbm_build_device(t.from_numpy(coords).cuda(), 8)
+    sides = [gu.to_dev(synth.sidecar_normal(g.n, C, seed=C)) for C in (1, 8)]
+    outs = [t.full_like(s, float("nan")) for s in sides]
+    vbm.vbm_box_filter_batch(g, sides, [1, 8], outs, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    for s, C, out in zip(sides, (1, 8), outs):
+        want = gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
+        np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C}")
 
 
 def test_fog_weno():
