@@ -268,9 +268,10 @@ __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const floa
 // decodes the block and builds each round's bricks once, then runs the gather
 // of every sidecar of the batch from them (channel counts with a compile-time
 // layout only, see batch_width).  Measured on the shell for C = 1, 3, 8, 16:
-// 240 us, against 312 us for four single-width launches and 262 us for one
+// 220 us, against 312 us for four single-width launches and 262 us for one
 // launch whose CTAs alternate between the sidecars.
 constexpr int kMaxBatch = VBM_MAX_BATCH;  // include/vbm.h
+constexpr int kFused = 4;                 // sidecars per launch
 struct BoxBatch {
     const float* sc[kMaxBatch];
     float* out[kMaxBatch];
@@ -295,10 +296,35 @@ __device__ __forceinline__ void round_gather(const BrickCtx& k, const BrickSmem&
     }
 }
 
-// One CTA per VBM block for all sidecars of the batch: the block is decoded
-// and each round's index bricks are built once, then every sidecar's gather
-// runs from the same bricks.
-__global__ void __launch_bounds__(512, 4) brick_box_shared_kernel(DevGrid g, BoxBatch a) {
+// The gather of sidecar E (< count) of the batch, its pointers passed as
+// restrict-qualified kernel parameters so that the compiler may move the next
+// voxel's loads above this voxel's stores (as in the single-width kernel;
+// taken from a struct the pointers cost 10-15% of the gather's time).
+template <int E>
+__device__ __forceinline__ void gather_entry(const BrickCtx& k, const BrickSmem& m, uint32_t l0, uint32_t sb,
+                                             uint32_t se, const BoxBatch& a, const float* __restrict__ sc,
+                                             float* __restrict__ out) {
+    if (E >= a.count) return;
+    switch (a.C[E]) {  // uniform per CTA
+        case 1: round_gather<1, false, 1>(k, m, l0, sb, se, 1, sc, out, 1); break;
+        case 2: round_gather<2, false, 2>(k, m, l0, sb, se, 1, sc, out, 2); break;
+        case 3: round_gather<3, false, 3>(k, m, l0, sb, se, 1, sc, out, 3); break;
+        case 4: round_gather<4, true, 4>(k, m, l0, sb, se, 1, sc, out, 4); break;
+        case 8: round_gather<4, true, 8>(k, m, l0, sb, se, 2, sc, out, 8); break;
+        case 16: round_gather<4, true, 16>(k, m, l0, sb, se, 4, sc, out, 16); break;
+        default: break;
+    }
+}
+
+// One CTA per VBM block for up to kFused sidecars: the block is decoded and
+// each round's index bricks are built once, then every sidecar's gather runs
+// from the same bricks.  40 registers (3 CTAs of 512 threads per SM): with
+// the restrict-qualified pointers the extra registers hold more loads in
+// flight (32 registers, 4 CTAs per SM, measured 8% slower).
+__global__ void __launch_bounds__(512, 3) brick_box_shared_kernel(
+    DevGrid g, BoxBatch a, const float* __restrict__ s0, const float* __restrict__ s1,
+    const float* __restrict__ s2, const float* __restrict__ s3, float* __restrict__ o0, float* __restrict__ o1,
+    float* __restrict__ o2, float* __restrict__ o3) {
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
@@ -307,24 +333,16 @@ __global__ void __launch_bounds__(512, 4) brick_box_shared_kernel(DevGrid g, Box
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
         const uint32_t sb = m.starts[l0], se = m.starts[l0 + nb];
-        for (int e = 0; e < a.count; ++e) {
-            switch (a.C[e]) {  // uniform per CTA
-                case 1: round_gather<1, false, 1>(k, m, l0, sb, se, 1, a.sc[e], a.out[e], 1); break;
-                case 2: round_gather<2, false, 2>(k, m, l0, sb, se, 1, a.sc[e], a.out[e], 2); break;
-                case 3: round_gather<3, false, 3>(k, m, l0, sb, se, 1, a.sc[e], a.out[e], 3); break;
-                case 4: round_gather<4, true, 4>(k, m, l0, sb, se, 1, a.sc[e], a.out[e], 4); break;
-                case 8: round_gather<4, true, 8>(k, m, l0, sb, se, 2, a.sc[e], a.out[e], 8); break;
-                case 16: round_gather<4, true, 16>(k, m, l0, sb, se, 4, a.sc[e], a.out[e], 16); break;
-                default: break;
-            }
-        }
+        gather_entry<0>(k, m, l0, sb, se, a, s0, o0);
+        gather_entry<1>(k, m, l0, sb, se, a, s1, o1);
+        gather_entry<2>(k, m, l0, sb, se, a, s2, o2);
+        gather_entry<3>(k, m, l0, sb, se, a, s3, o3);
         __syncthreads();  // the next round overwrites the bricks
     }
     if (blockIdx.x == 0)
         for (int e = 0; e < a.count; ++e)
             for (uint32_t c = threadIdx.x; c < (uint32_t)a.C[e]; c += blockDim.x) a.out[e][c] = 0.0f;
 }
-
 
 // Raw taps through the index bricks.  SHAPE 27 (box) or 7 (cross).
 template <int SHAPE>
@@ -402,9 +420,22 @@ cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* con
             if (e != cudaSuccess) return e;
         }
     }
-    if (a.count == 0) return cudaSuccess;
-    brick_box_shared_kernel<<<g.n_blocks, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(g, a);
-    return cudaGetLastError();
+    // kFused sidecars per launch
+    for (int first = 0; first < a.count; first += kFused) {
+        BoxBatch part{};
+        part.count = min(kFused, a.count - first);
+        for (int i = 0; i < part.count; ++i) {
+            part.sc[i] = a.sc[first + i];
+            part.out[i] = a.out[first + i];
+            part.C[i] = a.C[first + i];
+        }
+        brick_box_shared_kernel<<<g.n_blocks, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(
+            g, part, part.sc[0], part.sc[1], part.sc[2], part.sc[3], part.out[0], part.out[1], part.out[2],
+            part.out[3]);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream) {
