@@ -62,7 +62,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms (the caller
+    keeps the GPU busy with the benchmarked step while sampling)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -99,7 +100,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -110,12 +111,17 @@ class ClockSampler:
                 mx = float(f[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for name, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(power) if power else None}
 
 
 def max_over_ranks(value: float, device=None) -> float:
@@ -198,6 +204,15 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # The same step, untimed, for ~0.6 s first, so that the 200 ms clock
+        # samples see the GPU under this load (the K timed steps alone last a
+        # few ms); then the K timed steps.
+        busy_until = time.perf_counter() + 0.6
+        while time.perf_counter() < busy_until:
+            for _ in range(50):
+                flush_buf.zero_()
+                launch_step()
+            torch.cuda.synchronize()
         t0 = time.perf_counter()
         step_evs = [timed_launch(launch_step) for _ in range(args.steps)]
         torch.cuda.synchronize()
