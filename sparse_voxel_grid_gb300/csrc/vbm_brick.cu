@@ -148,6 +148,21 @@ __device__ __forceinline__ void gather_add_pred(float (&acc)[CC], const float* _
             acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
             acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], v.w);
         }
+    } else if constexpr (CC == 3) {
+        // A 12-byte row read as one 8-byte and one 4-byte load: the row's
+        // float offset f has the parity of idx*stride + ch0, and the sidecar
+        // is 16-byte aligned, so the 8-byte pair is (f, f+1) when f is even
+        // and (f+1, f+2) when f is odd.  Two loads per tap instead of three.
+        const bool odd = ((idx * stride + (uint32_t)ch0) & 1u) != 0u;
+        float s = 0.0f;
+        float2 p = make_float2(0.0f, 0.0f);
+        if (idx) {
+            s = __ldg(row + (odd ? 0 : 2));
+            p = __ldg(reinterpret_cast<const float2*>(row + (odd ? 1 : 0)));
+        }
+        acc[0] = __fadd_rn(acc[0], odd ? s : p.x);
+        acc[1] = __fadd_rn(acc[1], odd ? p.x : p.y);
+        acc[2] = __fadd_rn(acc[2], odd ? p.y : s);
     } else {
 #pragma unroll
         for (int c = 0; c < CC; ++c) {
@@ -277,10 +292,18 @@ struct BoxBatch {
     float* out[kMaxBatch];
     int C[kMaxBatch];
     int count;
+    int pair[2];  // entries (0,1) / (2,3) are gathered in one pass (pairs_in_one_pass)
 };
 
 __host__ __device__ constexpr bool batch_width(int C) {
     return C == 1 || C == 2 || C == 3 || C == 4 || C == 8 || C == 16;
+}
+
+// Two one-lane widths whose gathers share one pass (the host orders a pair
+// by C).  C = 2 is left out: with its instances the kernel no longer fits
+// its 40 registers without spills.
+__host__ __device__ constexpr bool pairs_in_one_pass(int Ca, int Cb) {
+    return (Ca == 1 || Ca == 3) && (Cb == 1 || Cb == 3) && Ca <= Cb;
 }
 
 // The gathers of one round for one sidecar, through the round's index bricks.
@@ -316,6 +339,49 @@ __device__ __forceinline__ void gather_entry(const BrickCtx& k, const BrickSmem&
     }
 }
 
+// The gathers of two one-lane sidecars (C = 1 or 3) in one pass over the
+// round's voxels: each tap's index is read from the brick once for both, which
+// saves the second pass's index reads (32 voxels per warp load, ~2.3
+// wavefronts each from bank conflicts) and puts both rows' loads in flight
+// together (the S185 four-sidecar step: 0.219 -> 0.210 ms).  Each sidecar's
+// sums keep the tap order, so the results are those of two passes.
+template <int CA, int CB>
+__device__ __forceinline__ void round_gather_pair(const BrickCtx& k, const BrickSmem& m, uint32_t l0, uint32_t sb,
+                                                  uint32_t se, const float* __restrict__ sa, float* __restrict__ oa,
+                                                  const float* __restrict__ sbk, float* __restrict__ ob) {
+    for (uint32_t s = sb + threadIdx.x; s < se; s += blockDim.x) {
+        const uint32_t* ibk = m.ib + (uint32_t)(m.lof[s] - l0) * kCells;
+        const int cc = own_cell(m.offs[s]);
+        float acc_a[CA], acc_b[CB];
+#pragma unroll
+        for (int c = 0; c < CA; ++c) acc_a[c] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CB; ++c) acc_b[c] = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kBoxTaps; ++t) {
+            const uint32_t idx = ibk[cc + box_cell_delta(t)];
+            gather_add_pred<CA, false, CA>(acc_a, sa, idx, CA, 0);
+            gather_add_pred<CB, false, CB>(acc_b, sbk, idx, CB, 0);
+        }
+        const uint32_t index = 1u + k.b * k.W + s;
+        store_row<CA, false>(oa, index, CA, 0, acc_a);
+        store_row<CB, false>(ob, index, CB, 0, acc_b);
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void gather_pair_entry(const BrickCtx& k, const BrickSmem& m, uint32_t l0, uint32_t sb,
+                                                  uint32_t se, const BoxBatch& a, const float* __restrict__ sa,
+                                                  float* __restrict__ oa, const float* __restrict__ sbk,
+                                                  float* __restrict__ ob) {
+    switch (a.C[E] * 4 + a.C[E + 1]) {  // uniform per CTA
+        case 1 * 4 + 1: round_gather_pair<1, 1>(k, m, l0, sb, se, sa, oa, sbk, ob); break;
+        case 1 * 4 + 3: round_gather_pair<1, 3>(k, m, l0, sb, se, sa, oa, sbk, ob); break;
+        case 3 * 4 + 3: round_gather_pair<3, 3>(k, m, l0, sb, se, sa, oa, sbk, ob); break;
+        default: break;
+    }
+}
+
 // One CTA per VBM block for up to kFused sidecars: the block is decoded and
 // each round's index bricks are built once, then every sidecar's gather runs
 // from the same bricks.  40 registers (3 CTAs of 512 threads per SM): with
@@ -333,10 +399,18 @@ __global__ void __launch_bounds__(512, 3) brick_box_shared_kernel(
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
         const uint32_t sb = m.starts[l0], se = m.starts[l0 + nb];
-        gather_entry<0>(k, m, l0, sb, se, a, s0, o0);
-        gather_entry<1>(k, m, l0, sb, se, a, s1, o1);
-        gather_entry<2>(k, m, l0, sb, se, a, s2, o2);
-        gather_entry<3>(k, m, l0, sb, se, a, s3, o3);
+        if (a.pair[0]) {
+            gather_pair_entry<0>(k, m, l0, sb, se, a, s0, o0, s1, o1);
+        } else {
+            gather_entry<0>(k, m, l0, sb, se, a, s0, o0);
+            gather_entry<1>(k, m, l0, sb, se, a, s1, o1);
+        }
+        if (a.pair[1]) {
+            gather_pair_entry<2>(k, m, l0, sb, se, a, s2, o2, s3, o3);
+        } else {
+            gather_entry<2>(k, m, l0, sb, se, a, s2, o2);
+            gather_entry<3>(k, m, l0, sb, se, a, s3, o3);
+        }
         __syncthreads();  // the next round overwrites the bricks
     }
     if (blockIdx.x == 0)
@@ -409,17 +483,21 @@ cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* con
                                    float* const* outs, cudaStream_t stream) {
     BoxBatch a{};
     a.count = 0;
-    for (int i = 0; i < count; ++i) {
-        if (batch_width(C[i])) {  // fused
+    // Fused widths: C = 1, then C = 3 (so that they pair up), then the others.
+    for (int pass = 0; pass < 3; ++pass)
+        for (int i = 0; i < count; ++i) {
+            const int rank = C[i] == 1 ? 0 : C[i] == 3 ? 1 : 2;
+            if (!batch_width(C[i]) || rank != pass) continue;
             a.sc[a.count] = sidecars[i];
             a.out[a.count] = outs[i];
             a.C[a.count] = C[i];
             ++a.count;
-        } else {
+        }
+    for (int i = 0; i < count; ++i)
+        if (!batch_width(C[i])) {
             const cudaError_t e = launch_brick_kind<0>(g, sidecars[i], C[i], outs[i], stream);
             if (e != cudaSuccess) return e;
         }
-    }
     // kFused sidecars per launch
     for (int first = 0; first < a.count; first += kFused) {
         BoxBatch part{};
@@ -429,6 +507,8 @@ cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* con
             part.out[i] = a.out[first + i];
             part.C[i] = a.C[first + i];
         }
+        for (int h = 0; h < 2; ++h)
+            part.pair[h] = part.count >= 2 * h + 2 && pairs_in_one_pass(part.C[2 * h], part.C[2 * h + 1]);
         brick_box_shared_kernel<<<g.n_blocks, threads_for(g.log2w), brick_smem_bytes(g.log2w), stream>>>(
             g, part, part.sc[0], part.sc[1], part.sc[2], part.sc[3], part.out[0], part.out[1], part.out[2],
             part.out[3]);

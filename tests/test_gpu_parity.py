@@ -188,11 +188,14 @@ def test_box_16_byte_aligned_buffers(C):
         np.testing.assert_array_equal(gu.bits(obuf[shift:shift + m].cpu().numpy()), want)
 
 
-@pytest.mark.parametrize("widths", [(1, 3, 8, 16), (16, 1), (5, 2, 13, 4), (8,)])
+@pytest.mark.parametrize("widths", [(1, 3, 8, 16), (16, 1), (5, 2, 13, 4), (8,), (3, 1), (2, 3, 8), (1, 2, 3),
+                                    (3, 2, 1, 3, 2, 1, 16, 8)])
 @pytest.mark.parametrize("resolver", RESOLVERS)
 def test_box_filter_batch(case, widths, resolver):
     # one call filtering several sidecars equals separate calls, bit for bit;
-    # with the brick resolver the widths 1/2/3/4/8/16 share one launch
+    # with the brick resolver the widths 1/2/3/4/8/16 share a launch (up to
+    # four per launch), and two one-lane widths (C <= 3) share one pass: the
+    # sets cover every such pair, in either order, and a second launch
     t = gu.torch()
     _, coords, o = case
     for log2w in (6, 9):
