@@ -12,7 +12,11 @@
 //     (no tail wave);
 //   - the CTA stages the firstLeafID and jumpMap words of the blocks its range
 //     overlaps in shared memory, with per-word popcount prefixes, so the rank
-//     is a shared-memory lookup plus one popcount;
+//     is a shared-memory lookup plus one popcount.  One staging (three
+//     barriers) serves VBM_DECODE_STAGE chunks of 512 slots: with one per
+//     chunk, warps waited at the barriers more than on any load (decode on
+//     the 20.4M-slot grid D: 107 -> 96 us with eight chunks, 40 registers
+//     and 12 CTAs per SM; at 16 CTAs the 32-register cap spills);
 //   - each thread decodes pairs of consecutive slots (a, a+1), a even, in
 //     explicit stages (all leaf-record loads, then all mask-word loads, then
 //     the selects), so its chains overlap instead of running one after
@@ -38,12 +42,16 @@ namespace {
 #define VBM_DECODE_PAIRS 2
 #endif
 #ifndef VBM_DECODE_MIN_CTAS
-#define VBM_DECODE_MIN_CTAS 16
+#define VBM_DECODE_MIN_CTAS 12
+#endif
+#ifndef VBM_DECODE_STAGE
+#define VBM_DECODE_STAGE 8
 #endif
 constexpr int kDecodeThreads = 128;
 constexpr int kPairs = VBM_DECODE_PAIRS;                    // slot pairs per thread per chunk
 constexpr int kMaxRange = kDecodeThreads * 2 * kPairs;      // slots per chunk
-constexpr int kMaxBlocks = kMaxRange / 64 + 2;              // blocks a chunk can overlap
+constexpr int kStageRange = kMaxRange * VBM_DECODE_STAGE;   // slots per staging of block metadata
+constexpr int kMaxBlocks = kStageRange / 64 + 2;            // blocks a staged range can overlap
 constexpr int kMaxWords = 8;                                // jumpMap words per block (W = 512)
 
 // Position of the first set bit of leaf L's mask at word w or later (the leaf
@@ -67,9 +75,9 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
     // The CTA's range [r0, r1), even-aligned so that slot pairs start on even slots.
     const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta) & ~1u;
     const uint32_t r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta) & ~1u;
-    for (uint32_t s0 = r0; s0 < r1; s0 += kMaxRange) {  // uniform per CTA
-        const uint32_t s1 = min(r1, s0 + (uint32_t)kMaxRange);
-        const uint32_t b0 = s0 >> log2w, nb = ((s1 - 1u) >> log2w) - b0 + 1u;
+    for (uint32_t S0 = r0; S0 < r1; S0 += kStageRange) {  // uniform per CTA
+        const uint32_t S1 = min(r1, S0 + (uint32_t)kStageRange);
+        const uint32_t b0 = S0 >> log2w, nb = ((S1 - 1u) >> log2w) - b0 + 1u;
 
         // Stage 1: block metadata of the chunk into shared memory.
         for (uint32_t e = threadIdx.x; e < nb * (words + 1u); e += blockDim.x) {
@@ -95,6 +103,8 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
         // Each thread decodes pairs of slots (a, a+1), a even.  The first by
         // rank + select; the second is the next voxel: the next set bit of the
         // same leaf, or the first set bit of the next leaf when one starts there.
+        for (uint32_t s0 = S0; s0 < S1; s0 += kMaxRange) {  // uniform per CTA; no barrier between chunks
+        const uint32_t s1 = min(S1, s0 + (uint32_t)kMaxRange);
         uint32_t la[kPairs], lb[kPairs];
         uint4 blo[kPairs], bhi[kPairs];
 #pragma unroll
@@ -146,7 +156,8 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             reinterpret_cast<uint2*>(leaf_index)[a >> 1] = make_uint2(la[k], lb[k]);
             reinterpret_cast<ushort2*>(voxel_offset)[a >> 1] = make_ushort2((uint16_t)oa, (uint16_t)ob);
         }
-        __syncthreads();  // the next chunk overwrites the staged metadata
+        }
+        __syncthreads();  // the next staged range overwrites the metadata
     }
 }
 
