@@ -21,7 +21,9 @@
 //     explicit stages (all leaf-record loads, then all mask-word loads, then
 //     the selects), so its chains overlap instead of running one after
 //     another, and stores each pair with one 8-byte and one 4-byte store;
-//   - slot a ranks and selects; slot a+1 holds the next active voxel, so its
+//   - slot a ranks and selects; a+1 is in the same block and jumpMap word
+//     (a is even), so its leaf is a's plus jumpMap bit a+1 (decode on D:
+//     96 -> 91 us); slot a+1 holds the next active voxel, so its
 //     offset is the next set bit of the same mask word (one find-first-set;
 //     rarely a later word), or the first set bit of the next leaf when one
 //     starts there: the select of rank r+1 taken one step from rank r
@@ -94,10 +96,15 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             }
         }
         __syncthreads();
-        auto rank_leaf = [&](uint32_t slot) {  // leaf of a slot: firstLeafID + jumpMap rank
+        // Leaves of slots a and a+1 (a even, so both in one block and one
+        // jumpMap word): firstLeafID + jumpMap rank of a, plus 1 when a leaf
+        // starts at a+1 (jumpMap bit of a+1).
+        auto rank_pair = [&](uint32_t slot, uint32_t& leaf_a, uint32_t& leaf_b) {
             const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
+            const uint64_t word = s_jw[bl][ws];
             const uint64_t keep = (2ull << (s & 63u)) - 1ull;
-            return s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(s_jw[bl][ws] & keep);
+            leaf_a = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(word & keep);
+            leaf_b = leaf_a + (uint32_t)((word >> ((s & 63u) + 1u)) & 1ull);
         };
 
         // Each thread decodes pairs of slots (a, a+1), a even.  The first by
@@ -112,8 +119,9 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             const uint32_t a = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads);
             la[k] = lb[k] = kNone;
             if (a < s1 && a < g.n) {  // index = a + 1 <= N
-                la[k] = rank_leaf(a);
-                if (a + 1u < g.n) lb[k] = rank_leaf(a + 1u);
+                uint32_t next;
+                rank_pair(a, la[k], next);
+                if (a + 1u < g.n) lb[k] = next;
                 const uint4* base = reinterpret_cast<const uint4*>(g.leaves[la[k]].base);
                 blo[k] = __ldg(base);
                 bhi[k] = __ldg(base + 1);
