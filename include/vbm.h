@@ -232,9 +232,11 @@ int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out
  * of sidecars[i] with C[i] channels, for i < count (1..VBM_MAX_BATCH), each
  * exactly as vbm_box_filter(grid, sidecars[i], C[i], outs[i], resolver,
  * VBM_OUTPUT_STREAMED, stream) computes it.  With the brick resolver the
- * filters whose C is 1, 2, 3, 4, 8 or 16 run as one launch in which each block
- * is decoded and its index bricks built once for all of them; other widths
- * and resolvers launch one filter after another.
+ * filters whose C is 1, 2, 3, 4, 8 or 16 run in launches of up to four, in
+ * which each block is decoded and its index bricks built once for all of them
+ * (and a C=1 and a C=3 filter read each tap's index once for both); other
+ * widths and resolvers launch one filter after another.  The order of the
+ * entries does not change any result.
  * sidecars, C and outs are host arrays of `count` entries; no output may alias
  * a sidecar or another output.  Errors: as vbm_box_filter, INVALID for a bad
  * count or aliasing. */
