@@ -244,7 +244,9 @@ def run_gpu(args):
         dom_ms = ms_per_step
         dom_bytes = sum(algorithmic_bytes(n, info["n_leaves"], info["n_blocks"], W, C) for C in CS)
         traffic = load_traffic(f"box_{args.resolver}_batch_W{W}")
+        l1_wavefronts = load_traffic(f"box_{args.resolver}_batch_W{W}_l1_wavefronts")
     else:
+        l1_wavefronts = None
         dom = max(CS, key=lambda C: statistics.mean(per_c_ms[C]))
         dom_label = f"box filter ({args.resolver} resolver, streamed) C={dom}"
         dom_ms = statistics.mean(per_c_ms[dom])
@@ -263,6 +265,15 @@ def run_gpu(args):
         cpu = cpu_baseline(coords, sample=args.cpu_sample, workload=args.workload)
 
     clk = clocks.summary()
+    l1 = None
+    if l1_wavefronts and clk.get("sm_mhz"):
+        # The kernel's real bound: L1 data-pipe wavefronts per launch (committed
+        # ncu count) over the live launch time, against one wavefront per SM
+        # per clock at the sampled SM clock.
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        cap = dom_ms * 1e-3 * sms * clk["sm_mhz"] * 1e6
+        l1 = {"wavefronts_per_launch": l1_wavefronts, "peak": "1 wavefront / SM / clock",
+              "frac": l1_wavefronts / cap}
     line = {
         "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -273,7 +284,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": dom_label, "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes},
+                     else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes, "l1_data_pipe": l1},
         "detail": detail,
         "e2e": e2e,
         "gpu_launches": (1 if args.step == "batch" and args.resolver == "brick" else len(CS)) * args.steps,
