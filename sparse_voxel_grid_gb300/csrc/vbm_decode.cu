@@ -17,17 +17,18 @@
 //     chunk, warps waited at the barriers more than on any load (decode on
 //     the 20.4M-slot grid D: 107 -> 96 us with eight chunks, 40 registers
 //     and 12 CTAs per SM; at 16 CTAs the 32-register cap spills);
-//   - each thread decodes pairs of consecutive slots (a, a+1), a even, in
-//     explicit stages (all leaf-record loads, then all mask-word loads, then
-//     the selects), so its chains overlap instead of running one after
-//     another, and stores each pair with one 8-byte and one 4-byte store;
-//   - slot a ranks and selects; a+1 is in the same block and jumpMap word
-//     (a is even), so its leaf is a's plus jumpMap bit a+1 (decode on D:
-//     96 -> 91 us); slot a+1 holds the next active voxel, so its
-//     offset is the next set bit of the same mask word (one find-first-set;
-//     rarely a later word), or the first set bit of the next leaf when one
-//     starts there: the select of rank r+1 taken one step from rank r
-//     (decode on the 20.4M-slot grid D: 134 -> 107 us);
+//   - each thread decodes a group of kGroup (8) consecutive slots a .. a+7,
+//     a a multiple of 8, so the group lies in one block and one jumpMap word.
+//     Slot a ranks and selects; slot a+i's leaf is a's plus the jumpMap bits
+//     a+1 .. a+i, and its offset is the next set bit after slot a+i-1's (one
+//     find-first-set in the same mask word, rarely a later word) or the first
+//     set bit of the leaf that starts at a+i.  One rank and one select serve
+//     eight slots, and the group is stored with 16-byte stores (decode on the
+//     20.4M-slot grid D: 134 -> 107 us with pairs, whose second slot first
+//     took its own rank; 96 -> 91 us when it took its leaf from the same
+//     jumpMap word; 91 -> 74 us with groups of four, 67 us with eight);
+//   - the loads of the group's leaf record and mask word come first, then the
+//     select and the next-bit steps, so the chains of a warp's threads overlap;
 //   - the word search reads the leaf's directory in its pre-added form, the
 //     eight 32-bit per-word base indices (first index + set bits in the words
 //     before), two 128-bit loads and seven 32-bit compares against the slot's
@@ -40,8 +41,11 @@
 namespace vbm {
 namespace {
 
-#ifndef VBM_DECODE_PAIRS
-#define VBM_DECODE_PAIRS 2
+#ifndef VBM_DECODE_GROUP
+#define VBM_DECODE_GROUP 8
+#endif
+#ifndef VBM_DECODE_GROUPS
+#define VBM_DECODE_GROUPS 1
 #endif
 #ifndef VBM_DECODE_MIN_CTAS
 #define VBM_DECODE_MIN_CTAS 12
@@ -50,20 +54,28 @@ namespace {
 #define VBM_DECODE_STAGE 8
 #endif
 constexpr int kDecodeThreads = 128;
-constexpr int kPairs = VBM_DECODE_PAIRS;                    // slot pairs per thread per chunk
-constexpr int kMaxRange = kDecodeThreads * 2 * kPairs;      // slots per chunk
-constexpr int kStageRange = kMaxRange * VBM_DECODE_STAGE;   // slots per staging of block metadata
+constexpr int kGroup = VBM_DECODE_GROUP;                    // consecutive slots per group (2, 4 or 8)
+constexpr int kGroups = VBM_DECODE_GROUPS;                  // groups per thread per chunk
+constexpr int kMaxRange = kDecodeThreads * kGroup * kGroups;  // slots per chunk
+constexpr int kStageRange = 512 * VBM_DECODE_STAGE;         // slots per staging of block metadata
 constexpr int kMaxBlocks = kStageRange / 64 + 2;            // blocks a staged range can overlap
 constexpr int kMaxWords = 8;                                // jumpMap words per block (W = 512)
+static_assert(kGroup == 2 || kGroup == 4 || kGroup == 8, "slot groups of 2, 4 or 8");
+static_assert(kStageRange % kMaxRange == 0, "a staged range holds whole chunks");
 
 // Position of the first set bit of leaf L's mask at word w or later (the leaf
-// has one there).
-__device__ __forceinline__ uint32_t first_bit_from(const LeafRec* __restrict__ rec, uint32_t w) {
+// has one there); *cw / *cword receive that word's number and bits.
+__device__ __forceinline__ uint32_t first_bit_from(const LeafRec* __restrict__ rec, uint32_t w, uint32_t* cw,
+                                                   uint64_t* cword) {
+    uint64_t m = 0;
     for (; w < 7u; ++w) {
-        const uint64_t m = __ldg(&rec->mask[w]);
-        if (m) return 64u * w + (uint32_t)__ffsll((long long)m) - 1u;
+        m = __ldg(&rec->mask[w]);
+        if (m) break;
     }
-    return 64u * 7u + (uint32_t)__ffsll((long long)__ldg(&rec->mask[7])) - 1u;
+    if (w == 7u) m = __ldg(&rec->mask[7]);
+    *cw = w;
+    *cword = m;
+    return 64u * w + (uint32_t)__ffsll((long long)m) - 1u;
 }
 
 __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_kernel(DevGrid g, uint32_t n_cta, uint32_t* __restrict__ leaf_index,
@@ -74,14 +86,14 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
 
     const uint32_t log2w = (uint32_t)g.log2w, W = 1u << log2w, words = W >> 6;
     const uint64_t n_slots = (uint64_t)g.n_blocks << log2w;
-    // The CTA's range [r0, r1), even-aligned so that slot pairs start on even slots.
-    const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta) & ~1u;
-    const uint32_t r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta) & ~1u;
+    // The CTA's range [r0, r1), aligned to the slot groups.
+    const uint32_t r0 = (uint32_t)(n_slots * blockIdx.x / n_cta) & ~(uint32_t)(kGroup - 1);
+    const uint32_t r1 = (uint32_t)(n_slots * (blockIdx.x + 1) / n_cta) & ~(uint32_t)(kGroup - 1);
     for (uint32_t S0 = r0; S0 < r1; S0 += kStageRange) {  // uniform per CTA
         const uint32_t S1 = min(r1, S0 + (uint32_t)kStageRange);
         const uint32_t b0 = S0 >> log2w, nb = ((S1 - 1u) >> log2w) - b0 + 1u;
 
-        // Stage 1: block metadata of the chunk into shared memory.
+        // Block metadata of the staged range into shared memory.
         for (uint32_t e = threadIdx.x; e < nb * (words + 1u); e += blockDim.x) {
             const uint32_t bl = e / (words + 1u), k = e - bl * (words + 1u);
             if (k == 0) s_fl[bl] = __ldg(&g.first_leaf[b0 + bl]);
@@ -96,43 +108,41 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             }
         }
         __syncthreads();
-        // Leaves of slots a and a+1 (a even, so both in one block and one
-        // jumpMap word): firstLeafID + jumpMap rank of a, plus 1 when a leaf
-        // starts at a+1 (jumpMap bit of a+1).
-        auto rank_pair = [&](uint32_t slot, uint32_t& leaf_a, uint32_t& leaf_b) {
-            const uint32_t bl = (slot >> log2w) - b0, s = slot & (W - 1u), ws = s >> 6;
-            const uint64_t word = s_jw[bl][ws];
-            const uint64_t keep = (2ull << (s & 63u)) - 1ull;
-            leaf_a = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(word & keep);
-            leaf_b = leaf_a + (uint32_t)((word >> ((s & 63u) + 1u)) & 1ull);
-        };
 
-        // Each thread decodes pairs of slots (a, a+1), a even.  The first by
-        // rank + select; the second is the next voxel: the next set bit of the
-        // same leaf, or the first set bit of the next leaf when one starts there.
+        // Each thread decodes groups of kGroup consecutive slots a .. a+kGroup-1
+        // (a a multiple of kGroup, so the group lies in one block and one
+        // jumpMap word).  Slot a by rank + select; slot a+i's leaf is a's plus
+        // the jumpMap bits a+1 .. a+i, and its offset the next set bit after
+        // slot a+i-1's in the same leaf, or the first set bit of the leaf that
+        // starts at a+i.
         for (uint32_t s0 = S0; s0 < S1; s0 += kMaxRange) {  // uniform per CTA; no barrier between chunks
         const uint32_t s1 = min(S1, s0 + (uint32_t)kMaxRange);
-        uint32_t la[kPairs], lb[kPairs];
-        uint4 blo[kPairs], bhi[kPairs];
+        uint32_t lf[kGroups][kGroup];
+        uint4 blo[kGroups], bhi[kGroups];
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k) {
-            const uint32_t a = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads);
-            la[k] = lb[k] = kNone;
+        for (int k = 0; k < kGroups; ++k) {
+            const uint32_t a = s0 + (uint32_t)kGroup * (threadIdx.x + (uint32_t)k * kDecodeThreads);
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i) lf[k][i] = kNone;
             if (a < s1 && a < g.n) {  // index = a + 1 <= N
-                uint32_t next;
-                rank_pair(a, la[k], next);
-                if (a + 1u < g.n) lb[k] = next;
-                const uint4* base = reinterpret_cast<const uint4*>(g.leaves[la[k]].base);
+                const uint32_t bl = (a >> log2w) - b0, s = a & (W - 1u), ws = s >> 6;
+                const uint64_t word = s_jw[bl][ws];
+                const uint32_t sb = s & 63u;
+                lf[k][0] = s_fl[bl] + s_cum[bl][ws] + (uint32_t)__popcll(word & ((2ull << sb) - 1ull));
+#pragma unroll
+                for (int i = 1; i < kGroup; ++i)
+                    if (a + (uint32_t)i < g.n) lf[k][i] = lf[k][i - 1] + (uint32_t)((word >> (sb + (uint32_t)i)) & 1ull);
+                const uint4* base = reinterpret_cast<const uint4*>(g.leaves[lf[k][0]].base);
                 blo[k] = __ldg(base);
                 bhi[k] = __ldg(base + 1);
             }
         }
-        uint64_t word[kPairs];
-        uint32_t wsel[kPairs], r[kPairs];
+        uint64_t word[kGroups];
+        uint32_t wsel[kGroups], r[kGroups];
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k) {
-            if (la[k] == kNone) continue;
-            const uint32_t index = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads) + 1u;
+        for (int k = 0; k < kGroups; ++k) {
+            if (lf[k][0] == kNone) continue;
+            const uint32_t index = s0 + (uint32_t)kGroup * (threadIdx.x + (uint32_t)k * kDecodeThreads) + 1u;
             const uint32_t b[8] = {blo[k].x, blo[k].y, blo[k].z, blo[k].w, bhi[k].x, bhi[k].y, bhi[k].z, bhi[k].w};
             uint32_t w = 0, before = b[0];
 #pragma unroll
@@ -143,26 +153,47 @@ __global__ void __launch_bounds__(kDecodeThreads, VBM_DECODE_MIN_CTAS) decode_ke
             }
             wsel[k] = w;
             r[k] = index - before;
-            word[k] = __ldg(&g.leaves[la[k]].mask[w]);
+            word[k] = __ldg(&g.leaves[lf[k][0]].mask[w]);
         }
 #pragma unroll
-        for (int k = 0; k < kPairs; ++k) {
-            const uint32_t a = s0 + 2u * (threadIdx.x + (uint32_t)k * kDecodeThreads);
+        for (int k = 0; k < kGroups; ++k) {
+            const uint32_t a = s0 + (uint32_t)kGroup * (threadIdx.x + (uint32_t)k * kDecodeThreads);
             if (a >= s1) continue;
-            uint32_t oa = kNoOffset, ob = kNoOffset;
-            if (la[k] != kNone) {
-                const uint32_t bit = select64(word[k], r[k]);
-                oa = 64u * wsel[k] + bit;
-                if (lb[k] == la[k]) {  // the next set bit of the same leaf
-                    const uint64_t rest = bit == 63u ? 0ull : word[k] & (~0ull << (bit + 1u));
-                    ob = rest ? 64u * wsel[k] + (uint32_t)__ffsll((long long)rest) - 1u
-                              : first_bit_from(g.leaves + la[k], wsel[k] + 1u);
-                } else if (lb[k] != kNone) {  // a leaf starts at slot a+1
-                    ob = first_bit_from(g.leaves + lb[k], 0u);
+            uint32_t off[kGroup];
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i) off[i] = kNoOffset;
+            if (lf[k][0] != kNone) {
+                uint32_t cw = wsel[k];      // mask word of the last decoded slot
+                uint64_t cword = word[k];
+                off[0] = 64u * cw + select64(cword, r[k]);
+#pragma unroll
+                for (int i = 1; i < kGroup; ++i) {
+                    if (lf[k][i] == kNone) break;
+                    if (lf[k][i] == lf[k][i - 1]) {  // the next set bit of the same leaf
+                        const uint32_t bit = off[i - 1] & 63u;
+                        const uint64_t rest = bit == 63u ? 0ull : cword & (~0ull << (bit + 1u));
+                        off[i] = rest ? 64u * cw + (uint32_t)__ffsll((long long)rest) - 1u
+                                      : first_bit_from(g.leaves + lf[k][i], cw + 1u, &cw, &cword);
+                    } else {  // a leaf starts at slot a+i
+                        off[i] = first_bit_from(g.leaves + lf[k][i], 0u, &cw, &cword);
+                    }
                 }
             }
-            reinterpret_cast<uint2*>(leaf_index)[a >> 1] = make_uint2(la[k], lb[k]);
-            reinterpret_cast<ushort2*>(voxel_offset)[a >> 1] = make_ushort2((uint16_t)oa, (uint16_t)ob);
+            if constexpr (kGroup == 8) {
+                uint4* li = reinterpret_cast<uint4*>(leaf_index) + (a >> 2);
+                li[0] = make_uint4(lf[k][0], lf[k][1], lf[k][2], lf[k][3]);
+                li[1] = make_uint4(lf[k][4], lf[k][5], lf[k][6], lf[k][7]);
+                reinterpret_cast<uint4*>(voxel_offset)[a >> 3] =
+                    make_uint4(off[0] | (off[1] << 16), off[2] | (off[3] << 16), off[4] | (off[5] << 16),
+                               off[6] | (off[7] << 16));
+            } else if constexpr (kGroup == 4) {
+                reinterpret_cast<uint4*>(leaf_index)[a >> 2] = make_uint4(lf[k][0], lf[k][1], lf[k][2], lf[k][3]);
+                reinterpret_cast<uint2*>(voxel_offset)[a >> 2] =
+                    make_uint2(off[0] | (off[1] << 16), off[2] | (off[3] << 16));
+            } else {
+                reinterpret_cast<uint2*>(leaf_index)[a >> 1] = make_uint2(lf[k][0], lf[k][1]);
+                reinterpret_cast<ushort2*>(voxel_offset)[a >> 1] = make_ushort2((uint16_t)off[0], (uint16_t)off[1]);
+            }
         }
         }
         __syncthreads();  // the next staged range overwrites the metadata
