@@ -267,13 +267,8 @@ def run_gpu(args):
     clk = clocks.summary()
     l1 = None
     if l1_wavefronts and clk.get("sm_mhz"):
-        # The kernel's real bound: L1 data-pipe wavefronts per launch (committed
-        # ncu count) over the live launch time, against one wavefront per SM
-        # per clock at the sampled SM clock.
-        sms = torch.cuda.get_device_properties(local).multi_processor_count
-        cap = dom_ms * 1e-3 * sms * clk["sm_mhz"] * 1e6
-        l1 = {"wavefronts_per_launch": l1_wavefronts, "peak": "1 wavefront / SM / clock",
-              "frac": l1_wavefronts / cap}
+        l1 = l1_data_pipe(l1_wavefronts, dom_ms, torch.cuda.get_device_properties(local).multi_processor_count,
+                          clk["sm_mhz"])
     line = {
         "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -309,6 +304,14 @@ def workload_config(args, n, n_leaves, n_blocks, n_over, max_span, world):
             "n_blocks_over_cache": n_over, "max_span": max_span, "resolver": args.resolver, "output": "streamed",
             "l2": "flushed before every launch", "value_counts": "4*N voxels per step (one per channel width)",
             "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def l1_data_pipe(wavefronts, ms, sms, sm_mhz):
+    """The batched kernel's real bound: L1 data-pipe wavefronts per launch
+    (the committed ncu count) over the live launch time, against one wavefront
+    per SM per clock at the sampled SM clock."""
+    cap = ms * 1e-3 * sms * sm_mhz * 1e6
+    return {"wavefronts_per_launch": wavefronts, "peak": "1 wavefront / SM / clock", "frac": wavefronts / cap}
 
 
 def load_traffic(key):
