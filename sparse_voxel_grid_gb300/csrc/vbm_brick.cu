@@ -25,7 +25,7 @@
 //     per-word bases, i.e. the 9-bit directory pre-added to the leaf's first
 //     index), plus one rank for each of the two halo cells.  Only the x planes
 //     that the block's voxels of that leaf touch are built, and the rows of up
-//     to kMaxGroup leaves are built together, one row per thread.
+//     to max_group leaves are built together, one row per thread.
 //  3. The gather is channel-parallel: thread (voxel, channel group) reads the
 //     voxel's 27 tap indices from the brick at fixed offsets from its own cell,
 //     in tap order t = (di+1)*9 + (dj+1)*3 + (dk+1), and adds
@@ -34,8 +34,13 @@
 //
 // The adds per voxel and channel are the same as the other resolvers', in the
 // same order, so the results are identical bit for bit.  There is no
-// MaxCachedLeaves limit: blocks spanning more than kMaxGroup leaves are built
+// MaxCachedLeaves limit: blocks spanning more than max_group leaves are built
 // in several rounds.
+//
+// Several sidecars on one grid (brick_box_shared_kernel): the decode and the
+// index bricks do not depend on the sidecar, so one CTA per block builds them
+// once and runs up to four sidecars' gathers from them; a C=1 and a C=3
+// sidecar share one pass (each tap's index read once for both).
 #include "vbm_brick.cuh"
 #include "vbm_launch.h"
 #include "vbm_stencil.cuh"
