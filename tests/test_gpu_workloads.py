@@ -153,6 +153,28 @@ def test_decode_grid_full(bricks, log2w, method):
     assert sent.sum() == g.n_slots - o.n
 
 
+def test_decode_grid_box_filter_batch(bricks):
+    # the benchmarked call on the dense-leaf grid D (20.4M voxels, W=512): every
+    # output against the width filtered alone by the cached resolver, and a
+    # sample of each against the oracle
+    coords, o = bricks
+    t = gu.torch()
+    g = vbm.vbm_build(coords, 9)
+    cs = (1, 3, 8, 16)
+    host = {C: synth.sidecar_uniform(o.n, C, seed=40 + C) for C in cs}
+    sides = [gu.to_dev(host[C]) for C in cs]
+    outs = [t.full_like(s, float("nan")) for s in sides]
+    vbm.vbm_box_filter_batch(g, sides, list(cs), outs, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    which = _sample(o.n, k=3000, seed=4)
+    for s, C, out in zip(sides, cs, outs):
+        got = gu.bits(out.cpu().numpy())
+        np.testing.assert_array_equal(got, gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED)),
+                                      err_msg=f"C={C}")
+        want = gu.bits(o.box_filter(host[C], C, which=which)).reshape(-1, C)
+        np.testing.assert_array_equal(got.reshape(-1, C)[which], want, err_msg=f"C={C} against the oracle")
+
+
 def test_fog_box_filter():
     coords = synth.WORKLOADS["F"]()
     o = oracle.OracleGrid(coords)
