@@ -236,12 +236,16 @@ cudaError_t launch_decode(const DevGrid& g, uint32_t* leaf_index, uint16_t* voxe
     if (g.n_blocks == 0) return cudaSuccess;
     const uint64_t n_slots = (uint64_t)g.n_blocks << g.log2w;
     // One resident wave of CTAs, each with an equal share of the slots.
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    // Resident CTAs per SM, queried once (thread-safe initialisation); a
+    // failed query counts as one and its error is cleared, not reported.
+    static const int per_sm = [] {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecodeThreads, 0) != cudaSuccess || n < 1) n = 1;
-        per_sm = n;
-    }
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel, kDecodeThreads, 0) != cudaSuccess) {
+            cudaGetLastError();
+            n = 1;
+        }
+        return n < 1 ? 1 : n;
+    }();
     uint64_t n_cta = (uint64_t)(g.sm_count > 0 ? g.sm_count : 1) * (uint64_t)per_sm;
     const uint64_t max_cta = (n_slots + 63) / 64;  // at least 64 slots per CTA
     if (n_cta > max_cta) n_cta = max_cta;
