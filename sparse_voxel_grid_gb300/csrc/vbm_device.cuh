@@ -128,26 +128,21 @@ __device__ __forceinline__ uint32_t walk_index(const DevGrid& g, int32_t x, int3
 
 // ---------------------------------------------------------------------------
 // Cached neighbour-leaf table ([2263] "Summary": the block cooperatively stages
-// a per-leaf neighbour table in shared memory, built by all threads; a block
-// spans leaves firstLeafID .. firstLeafID + popcount(jumpMap)).  Entry
-// [l*27 + (dx+1)*9 + (dy+1)*3 + (dz+1)] is the id of the leaf whose origin is
-// origin(firstLeafID+l) + 8*(dx,dy,dz), or kNone.  Must be called by every
-// thread of the block; ends with a barrier.
+// a per-leaf neighbour table in shared memory, built by all threads; "Built on
+// the register-decode API": the staging derives what it needs from the block's
+// metadata -- its first leaf is firstLeafID and it spans 1 + popcount(jumpMap)
+// consecutive leaves).  Entry [l*27 + (dx+1)*9 + (dy+1)*3 + (dz+1)] is the id
+// of the leaf whose origin is origin(firstLeafID+l) + 8*(dx,dy,dz), or kNone.
+// The pages leave open how an entry is found; here it is copied from the
+// builder's neighbour row of that leaf (the same 27 ids in one 128-byte line),
+// so staging is one load per entry with no tree probe.  Must be called by
+// every thread of the block; ends with a barrier.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void stage_leaf_table(const DevGrid& g, uint32_t first_leaf, uint32_t span,
                                                  uint32_t* __restrict__ table) {
     for (uint32_t e = threadIdx.x; e < span * 27u; e += blockDim.x) {
         const uint32_t l = e / 27u, t = e - l * 27u;
-        const uint32_t L = first_leaf + l;
-        uint32_t id = L;
-        if (t != 13u) {
-            const LeafRec* rec = g.leaves + L;
-            const int32_t ox = __ldg(&rec->origin[0]) + 8 * ((int32_t)(t / 9u) - 1);
-            const int32_t oy = __ldg(&rec->origin[1]) + 8 * ((int32_t)((t / 3u) % 3u) - 1);
-            const int32_t oz = __ldg(&rec->origin[2]) + 8 * ((int32_t)(t % 3u) - 1);
-            id = find_leaf(g, ox, oy, oz);
-        }
-        table[e] = id;
+        table[e] = __ldg(&g.nbr[(size_t)(first_leaf + l) * kNbrStride + t]);
     }
     __syncthreads();
 }

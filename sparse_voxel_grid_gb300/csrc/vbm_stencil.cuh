@@ -11,16 +11,20 @@
 
 namespace vbm {
 
-// acc[ch] += sidecar[idx*C + ch0 + ch] for ch < CC, fp32 round-to-nearest;
-// VEC: the row is read as float4s (CC % 4 == 0, rows 16-byte aligned).
+// acc[ch] += (idx != 0 ? sidecar[idx*C + ch0 + ch] : +0.0f) for ch < CC.  The
+// load is predicated rather than branched around, so the loads of several taps
+// can be in flight at once; an inactive tap adds +0.0, which leaves an fp32
+// accumulator that started at +0.0 unchanged bit for bit (such a sum is never
+// -0.0), so the result equals skipping the tap.
 template <int CC, bool VEC>
-__device__ __forceinline__ void gather_add(float (&acc)[CC], const float* __restrict__ sc, uint32_t idx, int C,
-                                           int ch0) {
+__device__ __forceinline__ void gather_add_if(float (&acc)[CC], const float* __restrict__ sc, uint32_t idx, int C,
+                                              int ch0) {
     const float* row = sc + (size_t)idx * (size_t)C + ch0;
     if constexpr (VEC) {
 #pragma unroll
         for (int q = 0; q < CC / 4; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (idx) v = __ldg(reinterpret_cast<const float4*>(row) + q);
             acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], v.x);
             acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], v.y);
             acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
@@ -28,7 +32,11 @@ __device__ __forceinline__ void gather_add(float (&acc)[CC], const float* __rest
         }
     } else {
 #pragma unroll
-        for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], __ldg(row + ch));
+        for (int ch = 0; ch < CC; ++ch) {
+            float v = 0.0f;
+            if (idx) v = __ldg(row + ch);
+            acc[ch] = __fadd_rn(acc[ch], v);
+        }
     }
 }
 
@@ -61,6 +69,18 @@ __device__ __forceinline__ void store_row(float* __restrict__ out, uint32_t inde
     }
 }
 
+template <int V>
+struct IntC {
+    static constexpr int value = V;
+};
+
+// f(IntC<0>{}) .. f(IntC<8>{}) in order, each with a compile-time value.
+template <class F>
+__device__ __forceinline__ void static_for_9(F&& f) {
+    f(IntC<0>{}); f(IntC<1>{}); f(IntC<2>{}); f(IntC<3>{}); f(IntC<4>{});
+    f(IntC<5>{}); f(IntC<6>{}); f(IntC<7>{}); f(IntC<8>{});
+}
+
 // Resolves tap (di,dj,dk) of one decoded voxel.  TABLE: through the block's
 // staged neighbour-leaf table row of the voxel's leaf; otherwise by tree walk.
 template <bool TABLE>
@@ -88,11 +108,78 @@ struct TapResolver {
     }
 };
 
+// The z-row of a leaf's mask word `word` (first index `base`: the word's entry
+// of the 9-bit directory pre-added to the leaf's first index) that starts at
+// bit yb (a multiple of 8): its 8 bits, and the index of the row's first
+// voxel.  A row lies in one 32-bit half of the word.
+struct RowByte {
+    uint32_t byte, rb;
+};
+__device__ __forceinline__ RowByte row_byte(uint64_t word, uint32_t base, uint32_t yb) {
+    const uint32_t lo = (uint32_t)word, hi = (uint32_t)(word >> 32);
+    const bool up = yb >= 32u;
+    const uint32_t half = up ? hi : lo, sh = yb & 31u;
+    RowByte r;
+    r.byte = (half >> sh) & 0xFFu;
+    r.rb = base + (up ? (uint32_t)__popc(lo) : 0u) + (uint32_t)__popc(half & ((1u << sh) - 1u));
+    return r;
+}
+
+// The three taps (di,dj,-1), (di,dj,0), (di,dj,+1) of a voxel at in-leaf
+// position (x,y,z), through its leaf's staged table row.  The three positions
+// lie in one z-row of one mask word of one leaf -- the word of x+di, the row of
+// y+dj -- so one popcount below bit z ranks all three (the z-1 bit, when set,
+// is one of the bits below z; the z+1 bit follows z), except where z-1 or z+1
+// crosses the leaf's z face (z = 0 or 7; never both): that tap is the last or
+// first bit of the same row of the z neighbour leaf.  Written without branches
+// (the z neighbour chosen by a select, its loads predicated), so that the loads
+// of all nine columns can be in flight together.
+template <int DI, int DJ>
+__device__ __forceinline__ void cached_column(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ row,
+                                              int32_t x, int32_t y, int32_t z, uint32_t (&idx)[3]) {
+    const int32_t nx = x + DI, ny = y + DJ;
+    const int32_t sxy = ((nx >> 3) + 1) * 9 + ((ny >> 3) + 1) * 3;
+    const uint32_t w = (uint32_t)(nx & 7), yb = (uint32_t)(ny & 7) * 8u, zu = (uint32_t)z;
+    const uint32_t L0 = row[sxy + 1];
+    const bool lo = zu == 0u, hi = zu == 7u;
+    const uint32_t Le = lo ? row[sxy] : hi ? row[sxy + 2] : kNone;
+    uint64_t word = 0, worde = 0;
+    uint32_t base = 0, basee = 0;
+    if (L0 != kNone) {
+        word = __ldg(&leaves[L0].mask[w]);
+        base = __ldg(&leaves[L0].base[w]);
+    }
+    if (Le != kNone) {
+        worde = __ldg(&leaves[Le].mask[w]);
+        basee = __ldg(&leaves[Le].base[w]);
+    }
+    const RowByte r = row_byte(word, base, yb), e = row_byte(worde, basee, yb);
+    // bits z-1, z, z+1 of the row as bits 0, 1, 2 (0 past either end of the row)
+    const uint32_t b3 = ((r.byte << 1) >> zu) & 7u;
+    const uint32_t below = (uint32_t)__popc(r.byte & ((1u << zu) - 1u));
+    const uint32_t bz = (b3 >> 1) & 1u;
+    // the face-crossing tap: the last bit of the -z neighbour's row, or the first of the +z one's
+    const uint32_t te = lo ? (((e.byte >> 7) & 1u) ? e.rb + (uint32_t)__popc(e.byte) - 1u : 0u)
+                           : ((e.byte & 1u) ? e.rb : 0u);
+    idx[1] = bz ? r.rb + below : 0u;
+    idx[0] = lo ? te : ((b3 & 1u) ? r.rb + below - 1u : 0u);
+    idx[2] = hi ? te : ((b3 & 4u) ? r.rb + below + bz : 0u);
+}
+
+// The 27 box taps of one voxel in tap order, three at a time: column
+// c = (di+1)*3 + (dj+1) holds taps 3c, 3c+1, 3c+2.
+template <int C3>
+__device__ __forceinline__ void box_column(const DevGrid& g, const uint32_t* table_row, int32_t x, int32_t y,
+                                           int32_t z, uint32_t (&idx)[3]) {
+    cached_column<C3 / 3 - 1, C3 % 3 - 1>(g.leaves, table_row, x, y, z, idx);
+}
+
 // 27-tap box filter of one voxel ([2262] "What changed"): taps in order
 // t = (di+1)*9 + (dj+1)*3 + (dk+1); acc starts at +0.0; each non-zero tap adds
 // its sidecar row.  MAT: the 27 indices are resolved into a per-thread array
 // first (computeBoxStencil); otherwise each tap is consumed as it is resolved
-// (forEachBoxStencil).  Same adds in the same order either way.
+// (forEachBoxStencil; the cached form resolves a column of three taps, then
+// consumes them in order).  Same adds in the same order either way.
 template <int CC, bool VEC, bool TABLE, bool MAT>
 __device__ __forceinline__ void box_slot(const DevGrid& g, const uint32_t* table_row, const Slot& d, uint32_t index,
                                          const float* __restrict__ sc, float* __restrict__ out, int C, int ch0) {
@@ -100,18 +187,35 @@ __device__ __forceinline__ void box_slot(const DevGrid& g, const uint32_t* table
     float acc[CC];
 #pragma unroll
     for (int ch = 0; ch < CC; ++ch) acc[ch] = 0.0f;
-    if constexpr (MAT) {
+    if constexpr (TABLE) {
+        uint32_t st[MAT ? kBoxTaps : 3];
+        auto column = [&](auto c3) {
+            constexpr int c = decltype(c3)::value;
+            uint32_t col[3];
+            box_column<c>(g, table_row, resolve.x, resolve.y, resolve.z, col);
+            if constexpr (MAT) {
+                st[3 * c] = col[0]; st[3 * c + 1] = col[1]; st[3 * c + 2] = col[2];
+            } else {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) gather_add_if<CC, VEC>(acc, sc, col[k], C, ch0);
+            }
+        };
+        static_for_9(column);
+        if constexpr (MAT) {
+#pragma unroll
+            for (int t = 0; t < kBoxTaps; ++t) gather_add_if<CC, VEC>(acc, sc, st[t], C, ch0);
+        }
+    } else if constexpr (MAT) {
         uint32_t st[kBoxTaps];
 #pragma unroll
         for (int t = 0; t < kBoxTaps; ++t) st[t] = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
 #pragma unroll
-        for (int t = 0; t < kBoxTaps; ++t)
-            if (st[t]) gather_add<CC, VEC>(acc, sc, st[t], C, ch0);
+        for (int t = 0; t < kBoxTaps; ++t) gather_add_if<CC, VEC>(acc, sc, st[t], C, ch0);
     } else {
 #pragma unroll
         for (int t = 0; t < kBoxTaps; ++t) {
             const uint32_t idx = resolve(t / 9 - 1, (t / 3) % 3 - 1, t % 3 - 1);
-            if (idx) gather_add<CC, VEC>(acc, sc, idx, C, ch0);
+            gather_add_if<CC, VEC>(acc, sc, idx, C, ch0);
         }
     }
     store_row<CC, VEC>(out, index, C, ch0, acc);
@@ -125,21 +229,20 @@ __device__ __forceinline__ constexpr int cross_di(int j) { return j == 0 ? -1 : 
 __device__ __forceinline__ constexpr int cross_dj(int j) { return j == 1 ? -1 : j == 5 ? 1 : 0; }
 __device__ __forceinline__ constexpr int cross_dk(int j) { return j == 2 ? -1 : j == 4 ? 1 : 0; }
 
+// Box tap t of cross tap j: (cross_di+1)*9 + (cross_dj+1)*3 + (cross_dk+1).
+__device__ __forceinline__ constexpr int cross_box_tap(int j) {
+    return (cross_di(j) + 1) * 9 + (cross_dj(j) + 1) * 3 + (cross_dk(j) + 1);
+}
+
 // Stage row[l*7 + j] = leaf holding tap j's position when it leaves leaf
 // firstLeafID + l (entry 3: the leaf itself), for the block's spanned leaves
-// (the pages' 16 x 7 cross table).  Ends with a barrier.
+// (the pages' 16 x 7 cross table), copied from the face entries of the
+// builder's neighbour rows.  Ends with a barrier.
 __device__ __forceinline__ void stage_cross_table(const DevGrid& g, uint32_t first_leaf, uint32_t span,
                                                   uint32_t* __restrict__ table) {
     for (uint32_t e = threadIdx.x; e < span * (uint32_t)kCrossTaps; e += blockDim.x) {
         const uint32_t l = e / kCrossTaps, j = e - l * kCrossTaps;
-        const uint32_t L = first_leaf + l;
-        uint32_t id = L;
-        if (j != 3u) {
-            const LeafRec* rec = g.leaves + L;
-            id = find_leaf(g, __ldg(&rec->origin[0]) + 8 * cross_di((int)j), __ldg(&rec->origin[1]) + 8 * cross_dj((int)j),
-                           __ldg(&rec->origin[2]) + 8 * cross_dk((int)j));
-        }
-        table[e] = id;
+        table[e] = __ldg(&g.nbr[(size_t)(first_leaf + l) * kNbrStride + cross_box_tap((int)j)]);
     }
     __syncthreads();
 }
@@ -177,11 +280,7 @@ __device__ __forceinline__ void cross_consume(const uint32_t (&st)[kCrossTaps], 
 #pragma unroll
     for (int j = 0; j < kCrossTaps; ++j) {
         if (OP == VBM_CROSS_LAPLACIAN && j == 3) continue;  // the centre enters below
-        if (st[j]) {
-            load_row<CC, VEC>(v, sc, st[j], C, ch0);
-#pragma unroll
-            for (int ch = 0; ch < CC; ++ch) acc[ch] = __fadd_rn(acc[ch], v[ch]);
-        }
+        gather_add_if<CC, VEC>(acc, sc, st[j], C, ch0);
     }
     if constexpr (OP == VBM_CROSS_LAPLACIAN) {
         load_row<CC, VEC>(v, sc, index, C, ch0);
