@@ -5,12 +5,16 @@ Workload: the sphere shell of radius 185 and thickness 3 (183.5 <= |p| <= 186.5,
 interleaved channels.  One step = the 27-tap box filter (select-based decode +
 brick resolver + streamed gather/accumulate, fused) over every active voxel of
 four sidecars, C = 1, 3, 8 and 16, BlockWidth 512, in one
-vbm_box_filter_batch call: one launch whose CTAs alternate between the four
-sidecars (`--step separate`: four calls).  `value` counts each voxel once per
-sidecar: 4 * N voxels per step.  Each width is also timed alone (`detail`);
-the other resolvers (the pages' tree walk and cached table), both output
-modes, both block widths, the cross Laplacian, the WENO consumer, the decodes
-and the builders are timed in `variants`.
+vbm_box_filter_batch call: one launch in which each CTA decodes one VBM block,
+builds its index bricks once and runs all four sidecars' gathers from them
+(`--step separate`: four calls).  `value` counts each voxel once per sidecar:
+4 * N voxels per step.  Each width is also timed alone (`detail`); the
+one-channel filters that the stated target names (the pages' cached streamed
+resolver at W = 128 and 512, and the brick resolver) are timed against the
+least time of a kernel with their launch shape (`target`); the other
+resolvers (the pages' tree walk and cached table), both output modes, both
+block widths, the cross Laplacian, the WENO consumer, the decodes and the
+builders are timed in `variants`.
 
 Timing: each step (and each detail launch) is bracketed by CUDA events on the
 launching stream; L2 is flushed (a write of twice its size) before each,
@@ -254,6 +258,10 @@ def run_gpu(args):
         traffic = load_traffic(f"box_{args.resolver}_W{W}_C{dom}")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
+    target = None
+    if not args.no_target:
+        target = run_target(torch, vbm, coords, g, sidecars, outs, timed_launch, args, peak_gbs)
+
     # end to end through the public API: pinned host sidecar -> device -> filter -> host
     e2e = None
     if not args.no_e2e:
@@ -281,6 +289,7 @@ def run_gpu(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "alg_bytes_per_launch": dom_bytes, "l1_data_pipe": l1},
         "detail": detail,
+        "target": target,
         "e2e": e2e,
         "gpu_launches": (1 if args.step == "batch" and args.resolver == "brick" else len(CS)) * args.steps,
         "clocks": clk,
@@ -331,6 +340,57 @@ def load_traffic(key):
     if h.hexdigest() != d.get("source_sha1"):
         return None
     return d.get(key)
+
+
+def run_target(torch, vbm, coords, g512, sidecars, outs, timed_launch, args, peak_gbs):
+    """The stated target: the fused cached box filter at C=1 on the shell at
+    >= 60% of the HBM roofline.  Times the one-channel box filters it concerns
+    (the pages' cached streamed resolver at W = 128 and 512, and the brick
+    resolver at both widths) and, beside them, the probe kernels with the same
+    launch shape: an empty kernel (the least time any kernel of that shape
+    takes after an L2 flush), one that only loads each block's metadata, and
+    one that only follows the brick resolver's chain of dependent loads.
+    Median of --steps launches each, L2 flushed before every launch."""
+    reps = max(args.steps, 10)
+
+    def tmed(fn):
+        for _ in range(3):
+            timed_launch(fn)
+        evs = [timed_launch(fn) for _ in range(reps)]
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    grids = {512: g512}
+    if g512.info["block_width"] != 128:
+        grids[128] = vbm.vbm_build_device(torch.from_numpy(coords).cuda(), 7)
+    s1, o1 = sidecars[1], outs[1]
+    rows, floors = [], {}
+    for W in sorted(grids):
+        g = grids[W]
+        info = g.info
+        b = algorithmic_bytes(info["n_active"], info["n_leaves"], info["n_blocks"], W, 1)
+        for name, resolver in (("cached streamed", vbm.RESOLVE_CACHED), ("brick", vbm.RESOLVE_BRICK)):
+            ms = tmed(lambda: vbm.vbm_box_filter(g, s1, 1, o1, resolver, vbm.OUTPUT_STREAMED))
+            key = f"box_{name.split()[0]}_W{W}_C1"
+            rows.append({"kernel": f"box filter C=1, {name}", "W": W, "ms": round(ms, 5), "alg_bytes": b,
+                         "gbs": b / (ms * 1e-3) / 1e9, "frac": b / (ms * 1e-3) / 1e9 / peak_gbs,
+                         "thread_inst_per_voxel": load_traffic(key + "_thread_inst_per_voxel"),
+                         "dram_bytes": load_traffic(key)})
+        fl = {}
+        for kname, kind in (("empty", vbm.PROBE_EMPTY), ("metadata", vbm.PROBE_METADATA),
+                            ("chain", vbm.PROBE_CHAIN)):
+            fl[f"{kname}_ms"] = round(tmed(lambda: vbm.vbm_probe_launch(g, kind, s1)), 5)
+        fl["ctas"] = info["n_blocks"]
+        fl["frac_if_kernel_took_empty_ms"] = b / (fl["empty_ms"] * 1e-3) / 1e9 / peak_gbs
+        floors[f"W{W}"] = fl
+    for W, g in grids.items():
+        if g is not g512:
+            g.close()
+    return {"statement": "fused cached box filter, C=1, on the ~1.3M-voxel shell at >= 60% of the HBM roofline",
+            "peak_gbs": peak_gbs, "kernels": rows, "launch_floor": floors,
+            "how": "median of the event times of repeated launches, L2 flushed before each; alg_bytes as the "
+                   "headline (sidecar read + output write + leaf and block metadata); launch_floor: probe "
+                   "kernels of the same launch shape (include/vbm_probe.h)"}
 
 
 def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream, resolver):
@@ -605,6 +665,7 @@ def main():
     ap.add_argument("--variant-reps", type=int, default=5)
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-target", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step", choices=["batch", "separate"], default="batch",
                     help="the four widths in one vbm_box_filter_batch call (default) or four calls")

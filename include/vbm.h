@@ -37,7 +37,7 @@
  *     channels: row r at [r*C, r*C+C).  Row 0 (background) is never read as a
  *     tap; filters write it as +0.0 so an output can serve as the next sidecar.
  *     Rows of a filter output are written only by that call: out must not
- *     alias the sidecar.
+ *     overlap the sidecar (a shared byte is rejected with VBM_ERR_INVALID).
  *   - Limits: N < 2^31 (indices are 32-bit), |x|,|y|,|z| <= 2^30, C in 1..64,
  *     log2 block width in 6..9 (W = 64..512).
  */
@@ -149,9 +149,10 @@ int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, ui
 
 /* vbm_build_device without any device allocation.  No counterpart on the
  * pages: this is a library-level variant for callers that cannot call
- * cudaMalloc -- code that must run while other work is being captured into a
- * CUDA graph, or that lives inside an application whose device memory is
- * managed by an allocator it does not own.  Such a caller passes, besides the
+ * cudaMalloc -- code inside an application whose device memory belongs to an
+ * allocator it does not own, or code that runs while another host thread is
+ * capturing work into a CUDA graph (cudaMalloc may synchronise the device and
+ * is refused during a global-mode capture).  Such a caller passes, besides the
  * coordinates (device array of 3n int32), the output memory: `arena`, a
  * 256-byte aligned device buffer of `arena_bytes` bytes that receives the
  * grid's arrays.
@@ -160,18 +161,25 @@ int vbm_build_device(const int32_t* coords, uint64_t n, int log2_block_width, ui
  *     until the process exits.  Larger inputs fail with VBM_ERR_RANGE.
  *   - If `arena` is NULL or too small the call fails with VBM_ERR_RANGE; when
  *     `arena_needed` is not NULL it receives the bytes this grid needs (so a
- *     first call with arena_bytes = 0 is a size query).
+ *     first call with arena_bytes = 0 is a size query).  Every grid needs at
+ *     least 256 bytes, an empty one (n = 0) included.
  *   - The first call on each device looks up the static array's address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current; the lookup is
+ *     thread-safe, and a failed lookup is retried by the next call.  Make that
+ *     first call before any stream capture.
  *   - Every call uses the same static array, which keeps the previous call's
  *     contents (the call clears what must start empty).  Calls that overlap
  *     on the GPU -- on different streams or host threads -- race; serialise
  *     them.
- *   - The call synchronises `stream`.  The handle owns no device memory:
- *     vbm_destroy frees only the handle, and the caller frees `arena` after
- *     destroying it.  The handle keeps no host copies (vbm_leaf_export returns
- *     VBM_ERR_STATE); every compute call works on it as on any grid.
+ *   - The call reads small counts back to the host (cudaMemcpyAsync into host
+ *     memory, then cudaStreamSynchronize) between its kernels.  While another
+ *     thread captures a graph in cudaStreamCaptureModeGlobal, CUDA may refuse
+ *     such calls from this thread; a capture that runs beside this call
+ *     should use thread-local or relaxed mode.
+ *   - The handle owns no device memory: vbm_destroy frees only the handle, and
+ *     the caller frees `arena` after destroying it.  The handle keeps no host
+ *     copies (vbm_leaf_export returns VBM_ERR_STATE); every compute call works
+ *     on it as on any grid.
  * Requires |x|,|y|,|z| < 2^20.  Errors: INVALID, ALIGN, RANGE, DUPLICATE, CUDA. */
 int vbm_build_device_noalloc(const int32_t* coords, uint64_t n, int log2_block_width, uint32_t flags, void* arena,
                              uint64_t arena_bytes, uint64_t* arena_needed, void* stream, vbm_grid** out);
@@ -237,9 +245,9 @@ int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out
  * (and a C=1 and a C=3 filter read each tap's index once for both); other
  * widths and resolvers launch one filter after another.  The order of the
  * entries does not change any result.
- * sidecars, C and outs are host arrays of `count` entries; no output may alias
- * a sidecar or another output.  Errors: as vbm_box_filter, INVALID for a bad
- * count or aliasing. */
+ * sidecars, C and outs are host arrays of `count` entries; no output may
+ * overlap a sidecar or another output (sidecars may overlap each other).
+ * Errors: as vbm_box_filter, INVALID for a bad count or an overlap. */
 int vbm_box_filter_batch(const vbm_grid* grid, int count, const float* const* sidecars, const int* C,
                          float* const* outs, int resolver, void* stream);
 
@@ -269,7 +277,7 @@ int vbm_cross_filter(const vbm_grid* grid, const float* sidecar, int C, float* o
  * inside max(min(minus,0)^2, max(plus,0)^2); out[v] = x term + y term + z term
  * in that order.  All in fp32, each operation rounded separately (no FMA), so
  * every resolver gives the same bits.  Scale by 1/dx^2 for spacing dx.
- * phi and out: device arrays of N+1 floats (out may not alias phi); out[0] is
+ * phi and out: device arrays of N+1 floats (out may not overlap phi); out[0] is
  * written as +0.0.  resolver: VBM_RESOLVE_*.  Errors: INVALID, STATE, ALIGN,
  * CUDA. */
 int vbm_weno_filter(const vbm_grid* grid, const float* phi, float iso, float* out, int resolver, void* stream);

@@ -28,6 +28,9 @@ OUTPUT_STREAMED = _K["VBM_OUTPUT_STREAMED"]
 OUTPUT_MATERIALISED = _K["VBM_OUTPUT_MATERIALISED"]
 CROSS_LAPLACIAN = _K["VBM_CROSS_LAPLACIAN"]
 CROSS_SUM = _K["VBM_CROSS_SUM"]
+PROBE_EMPTY = _K["VBM_PROBE_EMPTY"]
+PROBE_METADATA = _K["VBM_PROBE_METADATA"]
+PROBE_CHAIN = _K["VBM_PROBE_CHAIN"]
 EXPORT = {
     "leaf_mask": (_K["VBM_EXPORT_LEAF_MASK"], np.uint64, 8),
     "leaf_prefix": (_K["VBM_EXPORT_LEAF_PREFIX"], np.uint64, 1),
@@ -46,7 +49,7 @@ SENTINEL_OFFSET = 0xFFFF
 __all__ = [
     "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
     "vbm_decode_sweep", "vbm_box_filter", "vbm_box_filter_batch", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
-    "vbm_weno_taps", "vbm_last_error",
+    "vbm_weno_taps", "vbm_last_error", "vbm_probe_launch",
 ]
 
 
@@ -250,6 +253,14 @@ def vbm_weno_taps(grid: Grid, taps, resolver: int = RESOLVE_CACHED, stream=None)
     import torch
     check(load().vbm_weno_taps(grid.handle, _dev_ptr(taps, torch.int32, (grid.n + 1) * WENO_TAPS, "taps"),
                                int(resolver), _stream_handle(stream)))
+
+
+def vbm_probe_launch(grid: Grid, kind: int, sidecar=None, stream=None) -> None:
+    """A measurement probe with the grid's filter launch shape (include/vbm_probe.h):
+    PROBE_EMPTY, PROBE_METADATA, or PROBE_CHAIN (reads `sidecar`, N+1 float32)."""
+    import torch
+    p = _dev_ptr(sidecar, torch.float32, grid.n + 1, "sidecar") if sidecar is not None else None
+    check(load().vbm_probe_launch(grid.handle, int(kind), p, _stream_handle(stream)))
 
 
 class HostPipeline:

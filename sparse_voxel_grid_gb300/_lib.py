@@ -10,7 +10,13 @@ import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvbm.so")
-HEADER = os.path.join(os.path.dirname(HERE), "include", "vbm.h")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+HEADER = os.path.join(INCLUDE, "vbm.h")
+HEADERS = [os.path.join(INCLUDE, f) for f in ("vbm.h", "vbm_probe.h")]
+
+
+def _header_text() -> str:
+    return "\n".join(open(h).read() for h in HEADERS)
 
 _lock = threading.Lock()
 _lib = None
@@ -23,9 +29,9 @@ class VbmError(RuntimeError):
 
 
 def header_constants() -> dict:
-    """#define NAME value pairs of include/vbm.h (integers only)."""
+    """#define NAME value pairs of the headers in include/ (integers only)."""
     out = {}
-    for m in re.finditer(r"^#define\s+(VBM_\w+)\s+\(?(-?\w+)u?\)?", open(HEADER).read(), re.M):
+    for m in re.finditer(r"^#define\s+(VBM_\w+)\s+\(?(-?\w+)u?\)?", _header_text(), re.M):
         try:
             out[m.group(1)] = int(m.group(2).rstrip("u"), 0)
         except ValueError:
@@ -34,8 +40,8 @@ def header_constants() -> dict:
 
 
 def header_functions() -> list:
-    """Names of the functions include/vbm.h declares."""
-    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(vbm_\w+)\s*\(", open(HEADER).read(), re.M)))
+    """Names of the functions the headers in include/ declare."""
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(vbm_\w+)\s*\(", _header_text(), re.M)))
 
 
 class VbmInfo(ctypes.Structure):
@@ -97,6 +103,8 @@ def load(path: str = LIB_PATH):
             lib.vbm_weno_filter.argtypes = [p, p, ctypes.c_float, p, i32, p]
             lib.vbm_weno_taps.restype = i32
             lib.vbm_weno_taps.argtypes = [p, p, i32, p]
+            lib.vbm_probe_launch.restype = i32
+            lib.vbm_probe_launch.argtypes = [p, i32, p, p]
             _lib = lib
     return _lib
 

@@ -8,6 +8,7 @@
 #include <new>
 #include <string>
 
+#include "../../include/vbm_probe.h"
 #include "vbm_internal.h"
 #include "vbm_launch.h"
 
@@ -27,6 +28,15 @@ int fail_cuda(const char* what, cudaError_t e) {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Whether the byte ranges [a, a + abytes) and [b, b + bbytes) share a byte.
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return abytes && bbytes && pa < pb + bbytes && pb < pa + abytes;
+}
+
+// Bytes of a sidecar or filter output of C channels: (N+1) rows.
+size_t rows_bytes(const vbm_grid* g, int C) { return (size_t)(g->n + 1) * (size_t)C * sizeof(float); }
 
 // Switches to the grid's device for the duration of a call.
 class DeviceGuard {
@@ -317,7 +327,8 @@ static int check_filter(const vbm_grid* g, const float* sidecar, int C, const fl
         return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
     if ((rc = check_ptr(sidecar, fn, "sidecar"))) return rc;
     if ((rc = check_ptr(out, fn, "out"))) return rc;
-    if ((const void*)sidecar == (const void*)out) return fail(VBM_ERR_INVALID, std::string(fn) + ": out aliases sidecar");
+    if (overlaps(sidecar, rows_bytes(g, C), out, rows_bytes(g, C)))
+        return fail(VBM_ERR_INVALID, std::string(fn) + ": out overlaps sidecar");
     return VBM_OK;
 }
 
@@ -347,10 +358,12 @@ int vbm_box_filter_batch(const vbm_grid* g, int count, const float* const* sidec
     for (int i = 0; i < count; ++i) {
         int rc = check_filter(g, sidecars[i], C[i], outs[i], resolver, fn);
         if (rc) return rc;
-        for (int j = 0; j < count; ++j) {
-            if (j != i && (const void*)outs[i] == (const void*)sidecars[j])
-                return fail(VBM_ERR_INVALID, std::string(fn) + ": an output aliases a sidecar");
-            if (j < i && outs[i] == outs[j]) return fail(VBM_ERR_INVALID, std::string(fn) + ": two outputs alias");
+        for (int j = 0; j < i; ++j) {
+            if (overlaps(outs[i], rows_bytes(g, C[i]), sidecars[j], rows_bytes(g, C[j])) ||
+                overlaps(outs[j], rows_bytes(g, C[j]), sidecars[i], rows_bytes(g, C[i])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": an output overlaps a sidecar");
+            if (overlaps(outs[i], rows_bytes(g, C[i]), outs[j], rows_bytes(g, C[j])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": two outputs overlap");
         }
     }
     DeviceGuard guard(g->device);
@@ -433,6 +446,21 @@ int vbm_box_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) 
 int vbm_cross_taps(const vbm_grid* g, uint32_t* taps, int resolver, void* stream) {
     g_last_error.clear();
     return taps_common(g, taps, resolver, stream, false);
+}
+
+int vbm_probe_launch(const vbm_grid* g, int kind, const float* sidecar, void* stream) {
+    g_last_error.clear();
+    const char* fn = "vbm_probe_launch";
+    int rc = check_grid(g, fn);
+    if (rc) return rc;
+    if (kind != VBM_PROBE_EMPTY && kind != VBM_PROBE_METADATA && kind != VBM_PROBE_CHAIN)
+        return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown kind");
+    if (kind == VBM_PROBE_CHAIN && (rc = check_ptr(sidecar, fn, "sidecar"))) return rc;
+    if (g->n_blocks == 0) return VBM_OK;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
+    const cudaError_t e = vbm::launch_probe(g->dev, kind, sidecar, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_probe_launch: launch", e);
 }
 
 }  // extern "C"

@@ -480,6 +480,8 @@ cudaError_t launch_brick_kind(const DevGrid& g, const float* sc, int C, float* o
 
 }  // namespace
 
+size_t brick_box_smem_bytes(int log2w) { return brick_smem_bytes(log2w); }
+
 cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, float* out, cudaStream_t stream) {
     return launch_brick_kind<0>(g, sidecar, C, out, stream);
 }

@@ -552,12 +552,16 @@ constexpr NoAllocLayout kNoAlloc = noalloc_layout();
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAlloc.total];
 
 // Device address of the static scratch array, looked up once per device with
-// that device current.
+// that device current.  The lookup and the table are guarded by one mutex, so
+// first calls on the same device from several host threads are safe; a failed
+// lookup leaves the entry empty and is retried by the next call.
 constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
 cudaError_t noalloc_scratch(int device, unsigned char** out) {
     if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
     if (!g_noalloc_ptr[device]) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -658,7 +662,9 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
     const uint64_t n_blocks = (N + W - 1) / W;
     const ArenaLayout lay = arena_layout(nl, tot[1], tot[2], n_blocks, log2w);
     if (arena_needed) *arena_needed = lay.total;
-    if (!arena || arena_bytes < lay.total) {
+    // lay.total is at least 256 bytes (arena_layout), so a NULL arena is always
+    // too small, also for an empty grid.
+    if (arena_bytes < lay.total || !arena) {
         err = "vbm_build_device_noalloc: the arena holds " + std::to_string(arena_bytes) + " bytes; this grid needs " +
               std::to_string(lay.total);
         return VBM_ERR_RANGE;

@@ -33,6 +33,11 @@ cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, fl
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream);
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream);
 cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_t stream);
+// Dynamic shared memory of the brick box/cross kernels at block width 2^log2w.
+size_t brick_box_smem_bytes(int log2w);
+
+// Measurement probes (vbm_probe.cu, include/vbm_probe.h).
+cudaError_t launch_probe(const DevGrid& g, int kind, const float* sidecar, cudaStream_t stream);
 // Per-device kernel attributes (shared-memory opt-ins), set once when a grid
 // is created on the device, outside any stream capture.
 cudaError_t prepare_device_kernels(int device);

@@ -223,6 +223,21 @@ def test_box_filter_batch_errors():
     s2 = t.zeros(g.n + 1, device="cuda")
     with pytest.raises(vbm.VbmError):  # an output is another entry's sidecar
         vbm.vbm_box_filter_batch(g, [s, s2], [1, 1], [s2, o])
+    # partial overlaps: views of one buffer at different 16-byte offsets
+    big = t.zeros(4 * (g.n + 1) + 64, device="cuda")
+    a, b = big[: g.n + 1], big[4: g.n + 5]
+    c3 = big[8: 8 + 3 * (g.n + 1)]
+    with pytest.raises(vbm.VbmError, match="overlap"):  # two outputs share rows
+        vbm.vbm_box_filter_batch(g, [s, s2], [1, 1], [a, b])
+    with pytest.raises(vbm.VbmError, match="overlap"):  # an output shares rows with another entry's sidecar
+        vbm.vbm_box_filter_batch(g, [s, a], [1, 1], [o, b])
+    with pytest.raises(vbm.VbmError, match="overlap"):  # widths differ: C=3 output over a C=1 sidecar
+        vbm.vbm_box_filter_batch(g, [a, t.zeros(3 * (g.n + 1), device="cuda")], [1, 3], [o, c3])
+    # sidecars may share memory: both entries read the same rows
+    o2 = t.zeros(g.n + 1, device="cuda")
+    vbm.vbm_box_filter_batch(g, [a, a], [1, 1], [o, o2], vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    assert t.equal(o, o2)
 
 
 def test_empty_grid():
@@ -264,6 +279,11 @@ def test_device_errors():
     assert lib.vbm_box_filter(g.handle, ok, 0, ok, 1, 0, None) == -1
     assert lib.vbm_box_filter(g.handle, ok, 65, ok, 1, 0, None) == -1
     assert lib.vbm_box_filter(g.handle, ok, 1, ok, 1, 0, None) == -1  # aliasing
+    big = t.zeros(n + 1 + 8, dtype=t.float32, device="cuda")
+    part = ctypes.c_void_p(big.data_ptr() + 16)  # aligned, shares all but 4 rows with big
+    assert lib.vbm_box_filter(g.handle, ctypes.c_void_p(big.data_ptr()), 1, part, 1, 0, None) == -1
+    assert b"overlaps" in lib.vbm_last_error()
+    assert lib.vbm_weno_filter(g.handle, part, 0.0, ctypes.c_void_p(big.data_ptr()), 1, None) == -1
     assert lib.vbm_box_filter(g.handle, ok, 1, mis, 7, 0, None) == -1
     assert lib.vbm_cross_filter(g.handle, ok, 1, ok2, 1, 5, None) == -1
     assert b"op" in lib.vbm_last_error()
@@ -295,3 +315,20 @@ def test_host_pipeline_matches_direct_calls():
         for C in widths:
             want = o.box_filter(host_in[C].numpy(), C)
             np.testing.assert_array_equal(gu.bits(host_out[C].numpy()), gu.bits(want))
+
+
+def test_probe_launch():
+    """The measurement probes run with the filters' launch shape and leave the
+    grid and the sidecar untouched; bad arguments are rejected."""
+    t = gu.torch()
+    g = vbm.vbm_build(SMALL["tiny_shell"](), 7)
+    s = gu.to_dev(synth.sidecar_uniform(g.n, 1, seed=3))
+    before = s.clone()
+    for kind in (vbm.PROBE_EMPTY, vbm.PROBE_METADATA, vbm.PROBE_CHAIN):
+        vbm.vbm_probe_launch(g, kind, s)
+    t.cuda.synchronize()
+    assert t.equal(s, before)
+    lib = vbm.load()
+    assert lib.vbm_probe_launch(g.handle, 3, None, None) == -1
+    assert lib.vbm_probe_launch(g.handle, vbm.PROBE_CHAIN, None, None) == -1
+    assert lib.vbm_probe_launch(None, vbm.PROBE_EMPTY, None, None) == -1

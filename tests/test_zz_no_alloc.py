@@ -1,6 +1,7 @@
 """vbm_build_device_noalloc: the grid builder for callers that cannot allocate
-device memory (code running during CUDA-graph capture, or inside an
-application whose device memory belongs to an allocator it does not own).
+device memory (code inside an application whose device memory belongs to an
+allocator it does not own, or code running while another thread captures a
+CUDA graph, when cudaMalloc is refused).
 
 The entry point is called through the C ABI (ctypes) with caller-provided
 output memory, twice in a row on different inputs, and each grid it returns
@@ -89,3 +90,48 @@ def test_rejects_inputs_over_the_static_maximum():
     rc, g, need = _noalloc_build(cd, len(coords), 7, None, 0)
     assert rc == _lib.header_constants()["VBM_ERR_RANGE"] and g is None
     assert "65536" in vbm.vbm_last_error()
+
+
+def test_second_call_allocates_no_device_memory():
+    """After the first call on the device (which looks up the static array and
+    loads the kernels), a call with the same input changes the device's free
+    memory by not one byte."""
+    t = gu.torch()
+    coords = synth.WORKLOADS["T"]()
+    cd = t.from_numpy(coords).cuda()
+    rc, g, need = _noalloc_build(cd, len(coords), 7, None, 0)
+    assert g is None and need > 0
+    arenas = [t.empty(need, dtype=t.uint8, device="cuda") for _ in range(2)]
+    rc, g1, _ = _noalloc_build(cd, len(coords), 7, arenas[0], need)
+    assert rc == 0, vbm.vbm_last_error()
+    t.cuda.synchronize()
+    free_before, _ = t.cuda.mem_get_info()
+    rc, g2, _ = _noalloc_build(cd, len(coords), 7, arenas[1], need)
+    t.cuda.synchronize()
+    free_after, _ = t.cuda.mem_get_info()
+    assert rc == 0, vbm.vbm_last_error()
+    assert free_after == free_before, (free_before, free_after)
+    ref = vbm.vbm_build_device(cd, 7)
+    _check_same(g2, ref)
+    _check_same(g1, ref)
+    for g_ in (g1, g2, ref):
+        g_.close()
+
+
+def test_empty_input_needs_a_small_arena():
+    """n = 0: the size query asks for a non-empty arena (256 bytes), and the
+    empty grid built in it filters like any empty grid (row 0 written as +0.0)."""
+    t = gu.torch()
+    cd = t.zeros((0, 3), dtype=t.int32, device="cuda")
+    rc, g, need = _noalloc_build(cd, 0, 7, None, 0)
+    assert rc == _lib.header_constants()["VBM_ERR_RANGE"] and g is None and need == 256
+    arena = t.empty(need, dtype=t.uint8, device="cuda")
+    rc, g, _ = _noalloc_build(cd, 0, 7, arena, need)
+    assert rc == 0, vbm.vbm_last_error()
+    assert g.n == 0 and g.n_slots == 0 and g.info["on_device"] == 1
+    s = t.ones(3, device="cuda")
+    out = t.full((3,), 5.0, device="cuda")
+    vbm.vbm_box_filter(g, s, 3, out, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    assert (out.cpu() == 0).all()
+    g.close()
