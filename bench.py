@@ -394,29 +394,62 @@ def run_target(torch, vbm, coords, g512, sidecars, outs, timed_launch, args, pea
 
 
 def run_e2e(torch, vbm, g, n, sidecars, outs, args, stream, resolver):
-    """The step through the public host API: pinned host sidecars in, pinned
-    host outputs back, every step (vbm.HostPipeline overlaps the copies of
-    one width with the filtering of another)."""
-    host_in = {C: sidecars[C].cpu().pin_memory() for C in CS}
-    host_out = {C: torch.empty_like(host_in[C]).pin_memory() for C in CS}
-    pipe = vbm.HostPipeline(g, CS, resolver)
-    for _ in range(max(1, args.warmup)):
-        pipe.run(host_in, host_out)
+    """The step through the library's host-buffer call: every step is one
+    vbm_box_filter_batch_host call on pinned host sidecars (copies in, the
+    batched filter, copies back, all inside the call; consecutive calls
+    overlap on the grid's staging sets); wall clock over K steps.  Beside it,
+    the host link's own copy rate for the same bytes (each direction alone,
+    then both at once), which bounds it."""
+    host_in = [sidecars[C].cpu().pin_memory() for C in CS]
+    host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+
+    def step():
+        vbm.vbm_box_filter_batch_host(g, host_in, list(CS), host_out, resolver, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        pipe.run(host_in, host_out)
-    pipe.synchronize()
+        step()
     torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    for C in CS:  # the copies really carried the filter outputs
-        assert torch.equal(host_out[C], outs[C].cpu()), "e2e output differs from the device-timed output"
-    bi = sum(host_in[C].numel() * 4 for C in CS)
-    bo = sum(host_out[C].numel() * 4 for C in CS)
+    for C, h in zip(CS, host_out):  # the copies really carried the filter outputs
+        assert torch.equal(h, outs[C].cpu()), "e2e output differs from the device-timed output"
+    bi = sum(h.numel() * 4 for h in host_in)
+    bo = sum(h.numel() * 4 for h in host_out)
     return {"value": len(CS) * n / (ms * 1e-3), "unit": "voxels/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "how": "pinned host sidecars -> device -> box filter -> pinned host outputs each step, through "
-                   "sparse_voxel_grid_gb300.HostPipeline (copies overlapped with kernels on 3 streams); wall clock"}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "link": host_link(torch, bi, args.steps),
+            "how": "one vbm_box_filter_batch_host call per step (pinned host sidecars -> device -> batched box "
+                   "filter -> pinned host outputs, inside the library); wall clock over K steps"}
+
+
+def host_link(torch, nbytes, reps):
+    """Copy rate of the host link for `nbytes` each way (pinned host memory,
+    one cudaMemcpyAsync per direction per repetition): host to device alone,
+    device to host alone, and both at once on two streams.  GB/s."""
+    h_in = torch.empty(nbytes // 4, dtype=torch.float32).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    d_in = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    d_out = torch.empty_like(d_in)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def rate(h2d, d2h):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s1):
+                    d_in.copy_(h_in, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.synchronize()
+        return (h2d + d2h) * nbytes * reps / (time.perf_counter() - t0) / 1e9
+
+    rate(True, True)
+    return {"h2d_gbs": rate(True, False), "d2h_gbs": rate(False, True), "both_gbs": rate(True, True),
+            "bytes_each_way": nbytes}
 
 
 def run_variants(torch, vbm, coords, sidecars, outs, timed_launch, args):

@@ -251,6 +251,36 @@ int vbm_box_filter(const vbm_grid* grid, const float* sidecar, int C, float* out
 int vbm_box_filter_batch(const vbm_grid* grid, int count, const float* const* sidecars, const int* C,
                          float* const* outs, int resolver, void* stream);
 
+/* vbm_box_filter_batch on host-resident data: the end-to-end call for a
+ * caller whose sidecars and outputs live in host memory.  host_sidecars[i] and
+ * host_outs[i] are host arrays of (N+1)*C[i] floats (layout as on the device).
+ * The call copies every sidecar to the device (one cudaMemcpyAsync each), runs
+ * vbm_box_filter_batch on the device copies and copies every output back (one
+ * cudaMemcpyAsync each); the results are bit for bit those of
+ * vbm_box_filter_batch.  The copies and the filter run on the grid's own
+ * streams, and `stream` waits for the last copy back: the outputs are ready,
+ * and the host sidecars and outputs may be reused, once `stream` is
+ * synchronised.  The call itself only enqueues.  The copies in are not
+ * ordered after earlier work on `stream` (so that they overlap the previous
+ * call's filter and copies back): the host sidecars are read as they are when
+ * the copies run, and sidecars written by GPU work must be complete (that work
+ * synchronised) before the call.
+ *   - Device staging: the grid keeps two sets of device buffers (sidecars and
+ *     outputs of one call each) and alternates between them, so that the
+ *     copies of consecutive calls overlap the filter of the previous one.  A
+ *     set is allocated, or grown, by the first call that needs it (that call
+ *     allocates device memory and may wait for the set's previous use); calls
+ *     whose batches fit allocate nothing.  vbm_destroy frees the sets.
+ *   - Host memory: pinned memory (cudaHostAlloc, cudaHostRegister) gives
+ *     asynchronous copies that overlap in both directions; pageable memory is
+ *     accepted, and CUDA then copies synchronously with the calling thread.
+ *   - Calls on one grid from several host threads are serialised by a lock.
+ *   - No output may overlap a sidecar or another output (host byte ranges).
+ * Errors: as vbm_box_filter_batch (INVALID for NULL host pointers), NOMEM
+ * (staging allocation), CUDA. */
+int vbm_box_filter_batch_host(const vbm_grid* grid, int count, const float* const* host_sidecars, const int* C,
+                              float* const* host_outs, int resolver, void* stream);
+
 /* 7-tap cross stencil (centre and the six face neighbours, taps t in
  * {4,10,12,13,14,16,22} of the box numbering) consumed as `op`:
  * VBM_CROSS_LAPLACIAN: out = s - 6*centre, s = +0.0 plus each active face

@@ -48,7 +48,7 @@ SENTINEL_OFFSET = 0xFFFF
 
 __all__ = [
     "Grid", "VbmError", "vbm_build", "vbm_build_device", "vbm_destroy", "vbm_info", "vbm_leaf_export", "vbm_decode",
-    "vbm_decode_sweep", "vbm_box_filter", "vbm_box_filter_batch", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
+    "vbm_decode_sweep", "vbm_box_filter", "vbm_box_filter_batch", "vbm_box_filter_batch_host", "vbm_cross_filter", "vbm_weno_filter", "vbm_box_taps", "vbm_cross_taps",
     "vbm_weno_taps", "vbm_last_error", "vbm_probe_launch",
 ]
 
@@ -263,68 +263,39 @@ def vbm_probe_launch(grid: Grid, kind: int, sidecar=None, stream=None) -> None:
     check(load().vbm_probe_launch(grid.handle, int(kind), p, _stream_handle(stream)))
 
 
-class HostPipeline:
-    """Box-filters host-resident sidecars on the GPU with the copies overlapped.
-
-    For a fixed grid and a fixed list of channel widths, `run(host_in,
-    host_out)` copies each pinned host sidecar to the device, runs
-    vbm_box_filter on it and copies the output back.  Copies in each direction
-    are split into `copy_streams` contiguous chunks on their own streams (so
-    several copy engines work at once) and the kernels run on a third set, so
-    the copy of one sidecar overlaps the filtering of another and the copy-back
-    of a third; events order every reuse of a device buffer.  `run` only
-    enqueues: call `synchronize()` before reading host_out.
-    """
-
-    def __init__(self, grid: Grid, widths, resolver: int = RESOLVE_BRICK, output: int = OUTPUT_STREAMED,
-                 copy_streams: int = 1):
+def _host_ptr(a, numel: int, name: str) -> int:
+    """Address of a contiguous float32 host array (numpy or CPU torch tensor)."""
+    try:
         import torch
-        self.grid, self.widths, self.resolver, self.output = grid, tuple(widths), resolver, output
-        n = grid.n
-        self.k = max(1, int(copy_streams))
-        self.dev_in = {C: torch.empty((n + 1) * C, dtype=torch.float32, device="cuda") for C in self.widths}
-        self.dev_out = {C: torch.empty_like(self.dev_in[C]) for C in self.widths}
-        self.s_h2d = [torch.cuda.Stream() for _ in range(self.k)]
-        self.s_d2h = [torch.cuda.Stream() for _ in range(self.k)]
-        self.s_k = torch.cuda.Stream()
-        self.ev_in = {C: [torch.cuda.Event() for _ in range(self.k)] for C in self.widths}
-        self.ev_out = {C: [torch.cuda.Event() for _ in range(self.k)] for C in self.widths}
-        self.ev_k = {C: torch.cuda.Event() for C in self.widths}
-        self._primed = False
-        self.done = [torch.cuda.Event() for _ in range(self.k)]
+        if isinstance(a, torch.Tensor):
+            if a.is_cuda or a.dtype != torch.float32 or not a.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous float32 CPU tensor")
+            if a.numel() != numel:
+                raise ValueError(f"{name} must have {numel} elements, got {a.numel()}")
+            return a.data_ptr()
+    except ImportError:
+        pass
+    if not isinstance(a, np.ndarray) or a.dtype != np.float32 or not a.flags["C_CONTIGUOUS"]:
+        raise TypeError(f"{name} must be a contiguous float32 host array")
+    if a.size != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {a.size}")
+    return a.ctypes.data
 
-    def _chunks(self, numel: int):
-        step = (numel + self.k - 1) // self.k
-        step = (step + 3) // 4 * 4  # 16-byte aligned chunk starts
-        return [(i, min(i + step, numel)) for i in range(0, numel, step)]
 
-    def run(self, host_in: dict, host_out: dict) -> None:
-        import torch
-        for C in self.widths:
-            parts = self._chunks(self.dev_in[C].numel())
-            for j, (a, b) in enumerate(parts):
-                s = self.s_h2d[j]
-                if self._primed:
-                    s.wait_event(self.ev_k[C])      # the previous kernel has read dev_in[C]
-                with torch.cuda.stream(s):
-                    self.dev_in[C][a:b].copy_(host_in[C][a:b], non_blocking=True)
-                    self.ev_in[C][j].record(s)
-                self.s_k.wait_event(self.ev_in[C][j])
-            if self._primed:
-                for j in range(len(parts)):
-                    self.s_k.wait_event(self.ev_out[C][j])  # the previous copy-back has read dev_out[C]
-            vbm_box_filter(self.grid, self.dev_in[C], C, self.dev_out[C], self.resolver, self.output, self.s_k)
-            self.ev_k[C].record(self.s_k)
-            for j, (a, b) in enumerate(parts):
-                s = self.s_d2h[j]
-                s.wait_event(self.ev_k[C])
-                with torch.cuda.stream(s):
-                    host_out[C][a:b].copy_(self.dev_out[C][a:b], non_blocking=True)
-                    self.ev_out[C][j].record(s)
-        for j in range(self.k):
-            self.done[j].record(self.s_d2h[j])
-        self._primed = True
-
-    def synchronize(self) -> None:
-        for e in self.done:
-            e.synchronize()
+def vbm_box_filter_batch_host(grid: Grid, host_sidecars, Cs, host_outs, resolver: int = RESOLVE_BRICK,
+                              stream=None) -> None:
+    """vbm_box_filter_batch on host-resident (N+1)*C float32 arrays (numpy or
+    CPU torch tensors; pinned memory gives overlapped copies).  Only enqueues:
+    the outputs are ready once `stream` is synchronised (see include/vbm.h)."""
+    k = len(host_sidecars)
+    if not (len(Cs) == len(host_outs) == k):
+        raise ValueError("host_sidecars, Cs and host_outs must have the same length")
+    sc = (ctypes.c_void_p * max(k, 1))()
+    ou = (ctypes.c_void_p * max(k, 1))()
+    cs = (ctypes.c_int * max(k, 1))()
+    for i in range(k):
+        m = (grid.n + 1) * int(Cs[i])
+        sc[i] = _host_ptr(host_sidecars[i], m, "host sidecar")
+        ou[i] = _host_ptr(host_outs[i], m, "host output")
+        cs[i] = int(Cs[i])
+    check(load().vbm_box_filter_batch_host(grid.handle, k, sc, cs, ou, int(resolver), _stream_handle(stream)))

@@ -93,6 +93,8 @@ def load(path: str = LIB_PATH):
             lib.vbm_box_filter.argtypes = [p, p, i32, p, i32, i32, p]
             lib.vbm_box_filter_batch.restype = i32
             lib.vbm_box_filter_batch.argtypes = [p, i32, p, p, p, i32, p]
+            lib.vbm_box_filter_batch_host.restype = i32
+            lib.vbm_box_filter_batch_host.argtypes = [p, i32, p, p, p, i32, p]
             lib.vbm_cross_filter.restype = i32
             lib.vbm_cross_filter.argtypes = [p, p, i32, p, i32, i32, p]
             lib.vbm_box_taps.restype = i32

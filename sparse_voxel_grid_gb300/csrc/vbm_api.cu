@@ -228,10 +228,16 @@ int vbm_destroy(vbm_grid* g) {
     g_last_error.clear();
     if (!g) return VBM_OK;
     int rc = VBM_OK;
-    if (g->arena && g->owns_arena) {
+    if (g->hostio || (g->arena && g->owns_arena)) {  // host-only grids make no CUDA call
         DeviceGuard guard(g->device);
-        cudaError_t e = cudaFree(g->arena);
-        if (e != cudaSuccess) rc = fail_cuda("vbm_destroy: cudaFree", e);
+        if (g->hostio) {
+            vbm::destroy_host_io(g->hostio);
+            g->hostio = nullptr;
+        }
+        if (g->arena && g->owns_arena) {
+            cudaError_t e = cudaFree(g->arena);
+            if (e != cudaSuccess) rc = fail_cuda("vbm_destroy: cudaFree", e);
+        }
     }
     delete g;
     return rc;
@@ -368,17 +374,39 @@ int vbm_box_filter_batch(const vbm_grid* g, int count, const float* const* sidec
     }
     DeviceGuard guard(g->device);
     if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
-    if (g->n_blocks == 0) {
-        for (int i = 0; i < count && e == cudaSuccess; ++i) e = cudaMemsetAsync(outs[i], 0, sizeof(float) * (size_t)C[i], s);
-    } else if (resolver == VBM_RESOLVE_BRICK) {
-        e = vbm::launch_brick_box_batch(g->dev, count, sidecars, C, outs, s);
-    } else {
-        for (int i = 0; i < count && e == cudaSuccess; ++i)
-            e = vbm::launch_box_filter(g->dev, sidecars[i], C[i], outs[i], resolver, VBM_OUTPUT_STREAMED, s);
-    }
+    const cudaError_t e = vbm::launch_box_batch(g->dev, count, sidecars, C, outs, resolver,
+                                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter_batch: launch", e);
+}
+
+int vbm_box_filter_batch_host(const vbm_grid* cg, int count, const float* const* host_sidecars, const int* C,
+                              float* const* host_outs, int resolver, void* stream) {
+    g_last_error.clear();
+    const char* fn = "vbm_box_filter_batch_host";
+    int rc = check_grid(cg, fn);
+    if (rc) return rc;
+    if (count < 1 || count > VBM_MAX_BATCH) return fail(VBM_ERR_INVALID, std::string(fn) + ": count must be in 1..8");
+    if (!host_sidecars || !C || !host_outs) return fail(VBM_ERR_INVALID, std::string(fn) + ": NULL array");
+    if (resolver != VBM_RESOLVE_TREEWALK && resolver != VBM_RESOLVE_CACHED && resolver != VBM_RESOLVE_BRICK)
+        return fail(VBM_ERR_INVALID, std::string(fn) + ": unknown resolver");
+    for (int i = 0; i < count; ++i) {
+        if (C[i] < 1 || C[i] > vbm::kMaxC) return fail(VBM_ERR_INVALID, std::string(fn) + ": C must be in 1..64");
+        if (!host_sidecars[i] || !host_outs[i])
+            return fail(VBM_ERR_INVALID, std::string(fn) + ": a host sidecar or output is NULL");
+        for (int j = 0; j <= i; ++j) {
+            if (overlaps(host_outs[i], rows_bytes(cg, C[i]), host_sidecars[j], rows_bytes(cg, C[j])) ||
+                overlaps(host_outs[j], rows_bytes(cg, C[j]), host_sidecars[i], rows_bytes(cg, C[i])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": an output overlaps a sidecar");
+            if (j < i && overlaps(host_outs[i], rows_bytes(cg, C[i]), host_outs[j], rows_bytes(cg, C[j])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": two outputs overlap");
+        }
+    }
+    DeviceGuard guard(cg->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
+    std::string err;
+    rc = vbm::box_filter_batch_host(const_cast<vbm_grid*>(cg), count, host_sidecars, C, host_outs, resolver, stream,
+                                    err);
+    return rc == VBM_OK ? VBM_OK : fail(rc, err);
 }
 
 int vbm_cross_filter(const vbm_grid* g, const float* sidecar, int C, float* out, int resolver, int op,

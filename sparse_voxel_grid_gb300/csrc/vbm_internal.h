@@ -71,6 +71,10 @@ struct DevGrid {
     int sm_count;                // SMs of the grid's device (for one-wave launches)
 };
 
+// Device staging and streams of vbm_box_filter_batch_host (vbm_host.cu).
+struct HostIO;
+void destroy_host_io(HostIO* h);
+
 }  // namespace vbm
 
 struct vbm_grid {
@@ -99,6 +103,9 @@ struct vbm_grid {
     std::mutex mirror_mu;
     int device = -1;
     vbm::DevGrid dev{};
+    // vbm_box_filter_batch_host: staging buffers and streams, made on first use
+    std::mutex hostio_mu;
+    vbm::HostIO* hostio = nullptr;
 };
 
 namespace vbm {
@@ -157,6 +164,11 @@ int build_host(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, vbm
 // Fills the device arena and the host mirrors of g; synchronises `stream`.
 int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, void* stream, vbm_grid* g,
                  std::string& err);
+
+// vbm_box_filter_batch_host (vbm_host.cu): arguments already checked; the
+// grid's device is current.
+int box_filter_batch_host(vbm_grid* g, int count, const float* const* host_sidecars, const int* C,
+                          float* const* host_outs, int resolver, void* stream, std::string& err);
 
 // Allocation-free device builder (vbm_build_device_noalloc): temporary memory
 // in a static device array, the grid's arrays in the caller's `arena`.

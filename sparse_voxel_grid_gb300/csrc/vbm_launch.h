@@ -29,6 +29,11 @@ cudaError_t launch_brick_box(const DevGrid& g, const float* sidecar, int C, floa
 // share one launch, the others are launched one by one.
 cudaError_t launch_brick_box_batch(const DevGrid& g, int count, const float* const* sidecars, const int* C,
                                    float* const* outs, cudaStream_t stream);
+// Box filters of count sidecars on the device: the brick resolver's batched
+// launches, else one launch per sidecar; an empty grid writes row 0 only
+// (vbm_host.cu).
+cudaError_t launch_box_batch(const DevGrid& g, int count, const float* const* sidecars, const int* C,
+                             float* const* outs, int resolver, cudaStream_t stream);
 cudaError_t launch_brick_cross(const DevGrid& g, const float* sidecar, int C, float* out, int op, cudaStream_t stream);
 cudaError_t launch_brick_taps(const DevGrid& g, uint32_t* taps, int shape, cudaStream_t stream);
 cudaError_t launch_brick_weno(const DevGrid& g, const float* phi, float iso, float* out, cudaStream_t stream);

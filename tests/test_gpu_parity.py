@@ -192,20 +192,22 @@ def test_box_16_byte_aligned_buffers(C):
                                     (16, 8), (3, 2, 1, 3, 2, 1, 16, 8)])
 @pytest.mark.parametrize("resolver", RESOLVERS)
 def test_box_filter_batch(case, widths, resolver):
-    # one call filtering several sidecars equals separate calls, bit for bit;
-    # with the brick resolver the widths 1/2/3/4/8/16 share a launch (up to
-    # four per launch), and two one-lane widths (C <= 3) share one pass: the
-    # sets cover every such pair, in either order, and a second launch
+    # one call filtering several sidecars equals the oracle's box filter of each,
+    # bit for bit on every element; with the brick resolver the widths
+    # 1/2/3/4/8/16 share a launch (up to four per launch), and two one-lane
+    # widths (C <= 3) share one pass: the sets cover every such pair, in either
+    # order, and a second launch
     t = gu.torch()
     _, coords, o = case
+    hosts = [synth.sidecar_uniform(o.n, C, seed=10 + i) for i, C in enumerate(widths)]
+    wants = [gu.bits(o.box_filter(h, C)) for h, C in zip(hosts, widths)]
     for log2w in (6, 9):
         g = vbm.vbm_build(coords, log2w)
-        sides = [gu.to_dev(synth.sidecar_uniform(o.n, C, seed=10 + i)) for i, C in enumerate(widths)]
+        sides = [gu.to_dev(h) for h in hosts]
         outs = [t.full_like(s, float("nan")) for s in sides]
         vbm.vbm_box_filter_batch(g, sides, list(widths), outs, resolver)
         t.cuda.synchronize()
-        for s, C, out in zip(sides, widths, outs):
-            want = gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
+        for C, out, want in zip(widths, outs, wants):
             np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C} W=2^{log2w}")
 
 
@@ -298,23 +300,63 @@ def test_device_errors():
         assert fn(g.handle, ok, mis, None) == -6
 
 
-def test_host_pipeline_matches_direct_calls():
-    """HostPipeline (overlapped host<->device copies) returns the same bits as
-    vbm_box_filter on device tensors, on two runs in a row."""
+@pytest.mark.parametrize("resolver", [vbm.RESOLVE_BRICK, vbm.RESOLVE_CACHED])
+def test_box_filter_batch_host_matches_oracle(resolver):
+    """vbm_box_filter_batch_host (host sidecars in, host outputs back) equals
+    the oracle on every element, on three calls in a row with new data each
+    time (the grid's two staging sets used, then reused), with pinned torch
+    tensors and with pageable numpy arrays; a wider batch grows the staging."""
     t = gu.torch()
     coords = SMALL["tiny_shell"]()
     o = oracle.OracleGrid(coords)
     g = vbm.vbm_build(coords, 7)
-    widths = (1, 3, 8)
-    pipe = vbm.HostPipeline(g, widths)
-    for run in range(2):
-        host_in = {C: t.from_numpy(synth.sidecar_uniform(o.n, C, seed=run * 10 + C)).pin_memory() for C in widths}
-        host_out = {C: t.empty_like(host_in[C]).pin_memory() for C in widths}
-        pipe.run(host_in, host_out)
-        pipe.synchronize()
-        for C in widths:
-            want = o.box_filter(host_in[C].numpy(), C)
-            np.testing.assert_array_equal(gu.bits(host_out[C].numpy()), gu.bits(want))
+    widths = (1, 3, 8, 16)
+    for call in range(3):
+        pinned = call != 1
+        hosts = [synth.sidecar_uniform(o.n, C, seed=100 * call + C) for C in widths]
+        if pinned:
+            ins = [t.from_numpy(h).pin_memory() for h in hosts]
+            outs = [t.full((len(h),), float("nan")).pin_memory() for h in hosts]
+        else:
+            ins = hosts
+            outs = [np.full(len(h), np.nan, dtype=np.float32) for h in hosts]
+        vbm.vbm_box_filter_batch_host(g, ins, list(widths), outs, resolver)
+        t.cuda.current_stream().synchronize()
+        for h, C, out in zip(hosts, widths, outs):
+            got = out.numpy() if pinned else out
+            np.testing.assert_array_equal(gu.bits(got), gu.bits(o.box_filter(h, C)), err_msg=f"call {call} C={C}")
+    wide = (5, 24, 64)  # widths outside the fused layouts, and a larger staging set
+    hosts = [synth.sidecar_uniform(o.n, C, seed=7 + C) for C in wide]
+    outs = [np.empty_like(h) for h in hosts]
+    vbm.vbm_box_filter_batch_host(g, hosts, list(wide), outs, resolver)
+    t.cuda.current_stream().synchronize()
+    for h, C, out in zip(hosts, wide, outs):
+        np.testing.assert_array_equal(gu.bits(out), gu.bits(o.box_filter(h, C)), err_msg=f"C={C}")
+    g.close()
+
+
+def test_box_filter_batch_host_errors_and_empty_grid():
+    t = gu.torch()
+    g = vbm.vbm_build(SMALL["tiny_shell"](), 7)
+    h = np.zeros(g.n + 1, dtype=np.float32)
+    with pytest.raises(vbm.VbmError, match="overlap"):  # an output over the sidecar
+        vbm.vbm_box_filter_batch_host(g, [h], [1], [h])
+    big = np.zeros(2 * (g.n + 1), dtype=np.float32)
+    with pytest.raises(vbm.VbmError, match="overlap"):  # two outputs share rows
+        vbm.vbm_box_filter_batch_host(g, [h, h], [1, 1], [big[: g.n + 1], big[3: g.n + 4]])
+    lib = vbm.load()
+    import ctypes
+    arr = (ctypes.c_void_p * 1)(None)
+    cs = (ctypes.c_int * 1)(1)
+    assert lib.vbm_box_filter_batch_host(g.handle, 1, arr, cs, arr, vbm.RESOLVE_BRICK, None) == -1
+    assert b"NULL" in lib.vbm_last_error()
+    assert lib.vbm_box_filter_batch_host(g.handle, 0, arr, cs, arr, vbm.RESOLVE_BRICK, None) == -1
+    e = vbm.vbm_build(np.zeros((0, 3), dtype=np.int32), 7)
+    ins = [np.ones(3, dtype=np.float32)]
+    outs = [np.full(3, 5.0, dtype=np.float32)]
+    vbm.vbm_box_filter_batch_host(e, ins, [3], outs)
+    t.cuda.current_stream().synchronize()
+    assert (outs[0] == 0).all()
 
 
 def test_probe_launch():
