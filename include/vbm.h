@@ -281,6 +281,55 @@ int vbm_box_filter_batch(const vbm_grid* grid, int count, const float* const* si
 int vbm_box_filter_batch_host(const vbm_grid* grid, int count, const float* const* host_sidecars, const int* C,
                               float* const* host_outs, int resolver, void* stream);
 
+/* ---- Block-range shards (one grid, several GPUs) ----
+ * The path shards by VBM blocks: a block's voxels are consecutive indices and
+ * span few consecutive leaves ([2263] "Summary"), so a contiguous range of
+ * blocks owns a contiguous index range, and its box taps reach only the 27
+ * neighbour leaves of its own leaves.  Every rank keeps the whole topology
+ * (the grid), owns the sidecar rows of its index range, receives the rows of
+ * its halo from their owners, and filters its own blocks.  No counterpart on
+ * the pages (they run one GPU). */
+
+/* Shard s of n_shards owns blocks block_begin[s] .. block_begin[s+1]-1;
+ * block_begin (host, n_shards+1 entries) gets an even split of the blocks
+ * (which holds the voxel counts within one block of equal: every block but the
+ * last has W voxels).  Shard s then owns indices 1+block_begin[s]*W ..
+ * min(N, block_begin[s+1]*W).  Errors: INVALID (NULL, n_shards < 1). */
+int vbm_shard_blocks(const vbm_grid* grid, int n_shards, uint32_t* block_begin);
+
+/* Halo of the shard that owns blocks [b0, b1): the sorted indices, outside
+ * its own index range, of the active voxels of every leaf that is one of the
+ * 27 neighbours of a leaf its blocks span -- a superset of the indices its box
+ * (and cross) taps can reach.  Host computation from the grid's arrays (a
+ * device-built grid copies them to the host on first use).  rows (host) has
+ * room for `capacity` entries; *count receives the halo's size (a first call
+ * with capacity 0 is a size query; VBM_ERR_RANGE if capacity is smaller).
+ * Errors: INVALID (b0 >= b1 or b1 > n_blocks, NULL count), RANGE, STATE (a
+ * grid without host copies), NOMEM. */
+int vbm_shard_halo(const vbm_grid* grid, uint32_t b0, uint32_t b1, uint32_t* rows, uint64_t capacity,
+                   uint64_t* count);
+
+/* dst[k*C .. k*C+C) = src[rows[k]*C .. rows[k]*C+C) for k < count: the halo
+ * rows another shard needs, packed for the exchange.  src and dst are device
+ * arrays of floats, rows a device array of count uint32 (each < the rows of
+ * src, not checked).  Errors: INVALID, ALIGN, CUDA. */
+int vbm_gather_rows(const float* src, int C, const uint32_t* rows, uint64_t count, float* dst, void* stream);
+
+/* dst[rows[k]*C .. +C) = src[k*C .. +C) for k < count: received halo rows
+ * placed at their indices in the shard's sidecar (full (N+1)*C layout, only
+ * the shard's own rows and its halo rows defined).  Errors: as
+ * vbm_gather_rows. */
+int vbm_scatter_rows(const float* src, int C, const uint32_t* rows, uint64_t count, float* dst, void* stream);
+
+/* vbm_box_filter_batch restricted to the voxels of blocks [b0, b1): writes
+ * only their output rows (and row 0 if b0 == 0); reads only sidecar rows of
+ * those voxels and of their taps, i.e. the shard's own rows and its halo
+ * (vbm_shard_halo).  Same results, bit for bit, as the whole-grid call on
+ * those rows.  Errors: as vbm_box_filter_batch, INVALID for a bad range. */
+int vbm_box_filter_batch_blocks(const vbm_grid* grid, uint32_t b0, uint32_t b1, int count,
+                                const float* const* sidecars, const int* C, float* const* outs, int resolver,
+                                void* stream);
+
 /* 7-tap cross stencil (centre and the six face neighbours, taps t in
  * {4,10,12,13,14,16,22} of the box numbering) consumed as `op`:
  * VBM_CROSS_LAPLACIAN: out = s - 6*centre, s = +0.0 plus each active face

@@ -16,7 +16,7 @@ LIB = os.path.join(HERE, "libvbm.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["vbm_api.cu", "vbm_decode.cu", "vbm_box.cu", "vbm_cross.cu", "vbm_brick.cu", "vbm_weno.cu", "vbm_weno_brick.cu", "vbm_build_dev.cu", "vbm_probe.cu", "vbm_host.cu"]
+CU_SOURCES = ["vbm_api.cu", "vbm_decode.cu", "vbm_box.cu", "vbm_cross.cu", "vbm_brick.cu", "vbm_weno.cu", "vbm_weno_brick.cu", "vbm_build_dev.cu", "vbm_probe.cu", "vbm_host.cu", "vbm_shard.cu"]
 CPP_SOURCES = ["vbm_build.cpp"]
 
 

@@ -95,6 +95,16 @@ def load(path: str = LIB_PATH):
             lib.vbm_box_filter_batch.argtypes = [p, i32, p, p, p, i32, p]
             lib.vbm_box_filter_batch_host.restype = i32
             lib.vbm_box_filter_batch_host.argtypes = [p, i32, p, p, p, i32, p]
+            lib.vbm_shard_blocks.restype = i32
+            lib.vbm_shard_blocks.argtypes = [p, i32, p]
+            lib.vbm_shard_halo.restype = i32
+            lib.vbm_shard_halo.argtypes = [p, u32, u32, p, u64, ctypes.POINTER(u64)]
+            lib.vbm_gather_rows.restype = i32
+            lib.vbm_gather_rows.argtypes = [p, i32, p, u64, p, p]
+            lib.vbm_scatter_rows.restype = i32
+            lib.vbm_scatter_rows.argtypes = [p, i32, p, u64, p, p]
+            lib.vbm_box_filter_batch_blocks.restype = i32
+            lib.vbm_box_filter_batch_blocks.argtypes = [p, u32, u32, i32, p, p, p, i32, p]
             lib.vbm_cross_filter.restype = i32
             lib.vbm_cross_filter.argtypes = [p, p, i32, p, i32, i32, p]
             lib.vbm_box_taps.restype = i32

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <vector>
 #include <mutex>
 #include <new>
 #include <string>
@@ -407,6 +408,94 @@ int vbm_box_filter_batch_host(const vbm_grid* cg, int count, const float* const*
     rc = vbm::box_filter_batch_host(const_cast<vbm_grid*>(cg), count, host_sidecars, C, host_outs, resolver, stream,
                                     err);
     return rc == VBM_OK ? VBM_OK : fail(rc, err);
+}
+
+int vbm_shard_blocks(const vbm_grid* g, int n_shards, uint32_t* block_begin) {
+    g_last_error.clear();
+    if (!g || !block_begin) return fail(VBM_ERR_INVALID, "vbm_shard_blocks: NULL argument");
+    if (n_shards < 1) return fail(VBM_ERR_INVALID, "vbm_shard_blocks: n_shards must be at least 1");
+    for (int s = 0; s <= n_shards; ++s) block_begin[s] = (uint32_t)(g->n_blocks * (uint64_t)s / (uint64_t)n_shards);
+    return VBM_OK;
+}
+
+int vbm_shard_halo(const vbm_grid* g, uint32_t b0, uint32_t b1, uint32_t* rows, uint64_t capacity,
+                   uint64_t* count) {
+    g_last_error.clear();
+    const char* fn = "vbm_shard_halo";
+    if (!g || !count) return fail(VBM_ERR_INVALID, std::string(fn) + ": NULL argument");
+    *count = 0;
+    if (b0 > b1 || b1 > g->n_blocks) return fail(VBM_ERR_INVALID, std::string(fn) + ": bad block range");
+    if (!g->host_mirrors) return fail(VBM_ERR_STATE, std::string(fn) + ": this grid keeps no host copies");
+    if (int rc = fill_mirrors(g)) return rc;
+    std::vector<uint32_t> halo;
+    try {
+        vbm::shard_halo(g, b0, b1, halo);
+    } catch (const std::bad_alloc&) {
+        return fail(VBM_ERR_NOMEM, std::string(fn) + ": out of host memory");
+    }
+    *count = halo.size();
+    if (capacity < halo.size()) {
+        if (capacity == 0 && !rows) return VBM_OK;  // size query
+        return fail(VBM_ERR_RANGE, std::string(fn) + ": rows holds " + std::to_string(capacity) + " entries; the halo has " +
+                                       std::to_string(halo.size()));
+    }
+    if (!halo.empty()) {
+        if (!rows) return fail(VBM_ERR_INVALID, std::string(fn) + ": rows is NULL");
+        std::memcpy(rows, halo.data(), halo.size() * sizeof(uint32_t));
+    }
+    return VBM_OK;
+}
+
+static int rows_call(bool gather, const float* src, int C, const uint32_t* rows, uint64_t count, float* dst,
+                     void* stream) {
+    const char* fn = gather ? "vbm_gather_rows" : "vbm_scatter_rows";
+    if (C < 1 || C > vbm::kMaxC) return fail(VBM_ERR_INVALID, std::string(fn) + ": C must be in 1..64");
+    if (count == 0) return VBM_OK;
+    int rc;
+    if ((rc = check_ptr(src, fn, "src")) || (rc = check_ptr(rows, fn, "rows")) || (rc = check_ptr(dst, fn, "dst")))
+        return rc;
+    const cudaError_t e = vbm::launch_rows(gather, src, C, rows, count, dst, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda((std::string(fn) + ": launch").c_str(), e);
+}
+
+int vbm_gather_rows(const float* src, int C, const uint32_t* rows, uint64_t count, float* dst, void* stream) {
+    g_last_error.clear();
+    return rows_call(true, src, C, rows, count, dst, stream);
+}
+
+int vbm_scatter_rows(const float* src, int C, const uint32_t* rows, uint64_t count, float* dst, void* stream) {
+    g_last_error.clear();
+    return rows_call(false, src, C, rows, count, dst, stream);
+}
+
+int vbm_box_filter_batch_blocks(const vbm_grid* g, uint32_t b0, uint32_t b1, int count,
+                                const float* const* sidecars, const int* C, float* const* outs, int resolver,
+                                void* stream) {
+    g_last_error.clear();
+    const char* fn = "vbm_box_filter_batch_blocks";
+    int rc = check_grid(g, fn);
+    if (rc) return rc;
+    if (b0 > b1 || b1 > g->n_blocks) return fail(VBM_ERR_INVALID, std::string(fn) + ": bad block range");
+    if (count < 1 || count > VBM_MAX_BATCH) return fail(VBM_ERR_INVALID, std::string(fn) + ": count must be in 1..8");
+    if (!sidecars || !C || !outs) return fail(VBM_ERR_INVALID, std::string(fn) + ": NULL array");
+    for (int i = 0; i < count; ++i) {
+        if ((rc = check_filter(g, sidecars[i], C[i], outs[i], resolver, fn))) return rc;
+        for (int j = 0; j < i; ++j) {
+            if (overlaps(outs[i], rows_bytes(g, C[i]), sidecars[j], rows_bytes(g, C[j])) ||
+                overlaps(outs[j], rows_bytes(g, C[j]), sidecars[i], rows_bytes(g, C[i])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": an output overlaps a sidecar");
+            if (overlaps(outs[i], rows_bytes(g, C[i]), outs[j], rows_bytes(g, C[j])))
+                return fail(VBM_ERR_INVALID, std::string(fn) + ": two outputs overlap");
+        }
+    }
+    if (b0 == b1) return VBM_OK;
+    DeviceGuard guard(g->device);
+    if (!guard.ok()) return fail(VBM_ERR_CUDA, std::string(fn) + ": cannot select the grid's device");
+    vbm::DevGrid view = g->dev;
+    view.block0 = b0;
+    view.n_blocks = b1 - b0;
+    const cudaError_t e = vbm::launch_box_batch(view, count, sidecars, C, outs, resolver, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VBM_OK : fail_cuda("vbm_box_filter_batch_blocks: launch", e);
 }
 
 int vbm_cross_filter(const vbm_grid* g, const float* sidecar, int C, float* out, int resolver, int op,

@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float*
                                                          float* __restrict__ out, int C, int ch0) {
     __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kBoxTaps : 1];
     const uint32_t W = 1u << g.log2w, words = W >> 6;
-    const uint32_t b = blockIdx.x;
+    const uint32_t b = g.block0 + blockIdx.x;
     const uint64_t* jb = g.jump + (size_t)b * words;
     const uint32_t fl = __ldg(&g.first_leaf[b]);
     bool use_table = false;

@@ -280,7 +280,7 @@ template <int KIND, int CC, bool VEC, bool VALUES, int CT>
 __global__ void __launch_bounds__(512) brick_filter_kernel(DevGrid g, const float* __restrict__ sc,
                                                            float* __restrict__ out, int C, int ch_begin, int lanes) {
     extern __shared__ __align__(16) unsigned char smem[];
-    brick_filter_block<KIND, CC, VEC, VALUES, CT>(g, blockIdx.x, sc, out, C, ch_begin, lanes, smem);
+    brick_filter_block<KIND, CC, VEC, VALUES, CT>(g, g.block0 + blockIdx.x, sc, out, C, ch_begin, lanes, smem);
 }
 
 // Several box filters of one grid in one launch.  The decode and the index
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(512, 3) brick_box_shared_kernel(
     extern __shared__ __align__(16) unsigned char smem[];
     const BrickSmem m = carve(smem, g.log2w);
     BrickCtx k;
-    brick_prologue<false>(g, k, m.offs, m.lof, m.starts, blockIdx.x);
+    brick_prologue<false>(g, k, m.offs, m.lof, m.starts, g.block0 + blockIdx.x);
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
         build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(512, 3) brick_box_shared_kernel(
         }
         __syncthreads();  // the next round overwrites the bricks
     }
-    if (blockIdx.x == 0)
+    if (g.block0 + blockIdx.x == 0)
         for (int e = 0; e < a.count; ++e)
             for (uint32_t c = threadIdx.x; c < (uint32_t)a.C[e]; c += blockDim.x) a.out[e][c] = 0.0f;
 }

@@ -65,10 +65,12 @@ struct DevGrid {
     const uint32_t* nbr;         // n_leaves x kNbrStride: neighbour-leaf ids (see vbm_build.cpp)
     uint32_t n;                  // active voxels
     uint32_t n_leaves;
-    uint32_t n_blocks;
+    uint32_t n_blocks;           // blocks a launch covers (CTAs of a one-CTA-per-block kernel)
     uint32_t n_upper;
     int log2w;
     int sm_count;                // SMs of the grid's device (for one-wave launches)
+    uint32_t block0;             // first block a launch covers: CTA i filters block block0 + i
+                                 // (0 for whole-grid calls; a shard's first block otherwise)
 };
 
 // Device staging and streams of vbm_box_filter_batch_host (vbm_host.cu).
@@ -154,6 +156,7 @@ inline void set_device_views(vbm_grid* g, const ArenaLayout& a, int sm_count) {
     d.n_upper = g->n_upper;
     d.log2w = g->log2w;
     d.sm_count = sm_count;
+    d.block0 = 0;
 }
 
 // Host builder (vbm_build.cpp).  Fills every host array of g; returns a status
@@ -169,6 +172,10 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
 // grid's device is current.
 int box_filter_batch_host(vbm_grid* g, int count, const float* const* host_sidecars, const int* C,
                           float* const* host_outs, int resolver, void* stream, std::string& err);
+
+// Halo rows of the shard owning blocks [b0, b1) (vbm_shard.cu); the grid's
+// host arrays must be filled.
+void shard_halo(const vbm_grid* g, uint32_t b0, uint32_t b1, std::vector<uint32_t>& rows);
 
 // Allocation-free device builder (vbm_build_device_noalloc): temporary memory
 // in a static device array, the grid's arrays in the caller's `arena`.

@@ -41,6 +41,11 @@ cudaError_t launch_brick_weno_taps(const DevGrid& g, uint32_t* taps, cudaStream_
 // Dynamic shared memory of the brick box/cross kernels at block width 2^log2w.
 size_t brick_box_smem_bytes(int log2w);
 
+// Row gather (dst[k] = src[rows[k]]) or scatter (dst[rows[k]] = src[k]) of
+// C-float rows (vbm_shard.cu).
+cudaError_t launch_rows(bool gather, const float* src, int C, const uint32_t* rows, uint64_t count, float* dst,
+                        cudaStream_t stream);
+
 // Measurement probes (vbm_probe.cu, include/vbm_probe.h).
 cudaError_t launch_probe(const DevGrid& g, int kind, const float* sidecar, cudaStream_t stream);
 // Per-device kernel attributes (shared-memory opt-ins), set once when a grid

@@ -2,8 +2,11 @@
 
 Shell S185 (183.5 <= |p| <= 186.5, 1,290,538 voxels), the decode grid D
 (random 8^3 bricks on 512^3, ~20.4M voxels) and the fog F (value noise on
-512^3, ~36M voxels).  Decode maps are compared with the oracle in full; filter
-outputs on sampled voxels (the oracle computes them one by one), and all
+512^3, ~42.9M voxels).  Decode maps are compared with the oracle in full.  The
+benchmarked call (the device-built shell, W=512, four sidecars in one batched
+call) is compared with the oracle on every element, the oracle running on all
+host cores; other filter outputs on sampled voxels (every voxel of the fog's
+blocks that span more than MaxCachedLeaves leaves included), and all
 resolver/output variants must agree bit for bit on every voxel.
 """
 import numpy as np
@@ -13,6 +16,7 @@ import oracle
 import sparse_voxel_grid_gb300 as vbm
 import synth
 from tests import gpu_util as gu
+from tests import oracle_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +100,25 @@ def test_shell_box_filter_batch(shell):
         np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C}")
 
 
+def test_shell_benchmarked_call_every_element(shell):
+    """The benchmarked configuration exactly: the grid built on the device at
+    W=512, sidecars U[-1,1) seed 0 at C = 1, 3, 8, 16 in one
+    vbm_box_filter_batch call (brick resolver), every output element against
+    the oracle."""
+    coords, o = shell
+    t = gu.torch()
+    cs = (1, 3, 8, 16)
+    g = vbm.vbm_build_device(t.from_numpy(coords).cuda(), 9)
+    assert g.n == o.n
+    sides = [gu.to_dev(synth.sidecar_uniform(o.n, C, seed=0)) for C in cs]
+    outs = [t.full_like(s, float("nan")) for s in sides]
+    vbm.vbm_box_filter_batch(g, sides, list(cs), outs, vbm.RESOLVE_BRICK)
+    t.cuda.synchronize()
+    wants = oracle_pool.box_filter_all("S185", o.n, cs, seeds=(0, 0, 0, 0))
+    for C, out, want in zip(cs, outs, wants):
+        np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), gu.bits(want), err_msg=f"C={C}")
+
+
 def test_shell_laplacian(shell):
     coords, o = shell
     s = synth.sidecar_uniform(o.n, 1, seed=0)
@@ -175,12 +198,30 @@ def test_decode_grid_box_filter_batch(bricks):
         np.testing.assert_array_equal(got.reshape(-1, C)[which], want, err_msg=f"C={C} against the oracle")
 
 
-def test_fog_box_filter():
+def _over_cache_voxels(g, log2w):
+    """Indices of every voxel of the blocks that span more than MaxCachedLeaves
+    leaves (the cached resolver's tree-walk fallback)."""
+    jm = vbm.vbm_leaf_export(g, "block_jump")
+    spans = 1 + np.array([sum(bin(int(w)).count("1") for w in row) for row in jm])
+    W = 1 << log2w
+    blocks = np.nonzero(spans > vbm.MAX_CACHED_LEAVES)[0]
+    idx = np.concatenate([np.arange(1 + b * W, 1 + (b + 1) * W) for b in blocks]) if len(blocks) else np.zeros(0)
+    return blocks, idx[idx <= g.n].astype(np.int64)
+
+
+@pytest.fixture(scope="module")
+def fog():
     coords = synth.WORKLOADS["F"]()
-    o = oracle.OracleGrid(coords)
+    return coords, oracle.OracleGrid(coords)
+
+
+def test_fog_box_filter(fog):
+    coords, o = fog
     g = vbm.vbm_build(coords, 8)
     info = g.info
     assert info["n_active"] == o.n
+    blocks, over = _over_cache_voxels(g, 8)
+    assert len(blocks) == info["n_blocks_over_cache"] > 0
     C = 8
     s = synth.sidecar_normal(o.n, C, seed=0)
     sd = gu.to_dev(s)
@@ -189,27 +230,35 @@ def test_fog_box_filter():
     np.testing.assert_array_equal(cached, walk)
     brick = gu.bits(gu.box_filter(g, sd, C, vbm.RESOLVE_BRICK, vbm.OUTPUT_STREAMED))
     np.testing.assert_array_equal(brick, walk)
-    which = _sample(o.n, k=6000)
+    # every voxel of the over-cache blocks, and a sample of 60k others
+    which = np.union1d(_sample(o.n, k=60000), over)
     want = gu.bits(o.box_filter(s, C, which=which)).reshape(-1, C)
     np.testing.assert_array_equal(cached.reshape(-1, C)[which], want)
 
 
-def test_fog_box_filter_batch():
-    coords = synth.WORKLOADS["F"]()
+def test_fog_box_filter_batch(fog):
+    coords, o = fog
     t = gu.torch()
     g = vbm.vbm_build_device(t.from_numpy(coords).cuda(), 8)
-    sides = [gu.to_dev(synth.sidecar_normal(g.n, C, seed=C)) for C in (1, 8)]
+    _, over = _over_cache_voxels(g, 8)
+    assert len(over) > 0
+    hosts = {C: synth.sidecar_normal(g.n, C, seed=C) for C in (1, 8)}
+    sides = [gu.to_dev(hosts[C]) for C in (1, 8)]
     outs = [t.full_like(s, float("nan")) for s in sides]
     vbm.vbm_box_filter_batch(g, sides, [1, 8], outs, vbm.RESOLVE_BRICK)
     t.cuda.synchronize()
+    which = np.union1d(_sample(o.n, k=30000, seed=5), over)
     for s, C, out in zip(sides, (1, 8), outs):
+        got = gu.bits(out.cpu().numpy())
         want = gu.bits(gu.box_filter(g, s, C, vbm.RESOLVE_CACHED, vbm.OUTPUT_STREAMED))
-        np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), want, err_msg=f"C={C}")
+        np.testing.assert_array_equal(got, want, err_msg=f"C={C}")
+        np.testing.assert_array_equal(got.reshape(-1, C)[which],
+                                      gu.bits(o.box_filter(hosts[C], C, which=which)).reshape(-1, C),
+                                      err_msg=f"C={C} against the oracle")
 
 
-def test_fog_weno():
-    coords = synth.WORKLOADS["F"]()
-    o = oracle.OracleGrid(coords)
+def test_fog_weno(fog):
+    coords, o = fog
     g = vbm.vbm_build(coords, 8)
     phi = synth.sidecar_normal(o.n, 1, seed=3)
     phi[0] = 0.5
