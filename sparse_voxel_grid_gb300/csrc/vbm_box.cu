@@ -20,9 +20,13 @@
 namespace vbm {
 namespace {
 
-template <int CC, bool VEC, bool CACHED, bool MAT>
-__global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float* __restrict__ sc,
-                                                         float* __restrict__ out, int C, int ch0) {
+// One CTA per VBM block, one thread per slot.  CT > 0: the row stride C is the
+// compile-time CT (and ch0 is 0), so that the gathers' row addresses need no
+// multiply by a runtime channel count.
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+__device__ __forceinline__ void box_filter_block(const DevGrid& g, const float* __restrict__ sc,
+                                                 float* __restrict__ out, int C_rt, int ch0_rt) {
+    const int C = CT > 0 ? CT : C_rt, ch0 = CT > 0 ? 0 : ch0_rt;
     __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kBoxTaps : 1];
     const uint32_t W = 1u << g.log2w, words = W >> 6;
     const uint32_t b = g.block0 + blockIdx.x;
@@ -47,6 +51,39 @@ __global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float*
         box_slot<CC, VEC, false, MAT>(g, nullptr, d, index, sc, out, C, ch0);
     }
     if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
+}
+
+// The streamed one-lane forms (CC <= 3) run held to 40 registers (3 CTAs of 512
+// threads, 12 of 128, per SM): left free, the cached C=1 kernel takes 54 and
+// runs 7-15% slower with fewer CTAs resident.  The wider and materialised forms
+// would spill under that cap and keep the compiler's choice.
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+__global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float* __restrict__ sc,
+                                                         float* __restrict__ out, int C, int ch0) {
+    box_filter_block<CC, VEC, CACHED, MAT, CT>(g, sc, out, C, ch0);
+}
+
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+__global__ void __launch_bounds__(512, 3) box_filter_kernel_r40(DevGrid g, const float* __restrict__ sc,
+                                                                float* __restrict__ out, int C, int ch0) {
+    box_filter_block<CC, VEC, CACHED, MAT, CT>(g, sc, out, C, ch0);
+}
+
+// The materialised forms are held to 64 registers (2 CTAs of 512 threads per
+// SM): with a compile-time stride the C=16 ones otherwise take 78-82 and run
+// 11-28% slower.
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+__global__ void __launch_bounds__(512, 2) box_filter_kernel_r64(DevGrid g, const float* __restrict__ sc,
+                                                                float* __restrict__ out, int C, int ch0) {
+    box_filter_block<CC, VEC, CACHED, MAT, CT>(g, sc, out, C, ch0);
+}
+
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+void launch_box_kernel(dim3 grid, dim3 block, cudaStream_t stream, const DevGrid& g, const float* sc, float* out,
+                       int C, int ch0) {
+    if constexpr (MAT) box_filter_kernel_r64<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else if constexpr (CC <= 3) box_filter_kernel_r40<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else box_filter_kernel<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
 }
 
 // Raw taps: taps[index*27 + t].  Row 0 is zero.
@@ -81,15 +118,15 @@ __global__ void __launch_bounds__(512) box_taps_kernel(DevGrid g, uint32_t* __re
     if (b == 0 && threadIdx.x < (unsigned)kBoxTaps) taps[threadIdx.x] = 0u;
 }
 
-template <int CC, bool VEC>
+template <int CC, bool VEC, int CT = 0>
 cudaError_t launch_box_cc(const DevGrid& g, const float* sc, int C, int ch0, float* out, int resolver, int output,
                           cudaStream_t stream) {
     const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
     const bool cached = resolver == VBM_RESOLVE_CACHED, mat = output == VBM_OUTPUT_MATERIALISED;
-    if (cached && mat) box_filter_kernel<CC, VEC, true, true><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
-    else if (cached) box_filter_kernel<CC, VEC, true, false><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
-    else if (mat) box_filter_kernel<CC, VEC, false, true><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
-    else box_filter_kernel<CC, VEC, false, false><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    if (cached && mat) launch_box_kernel<CC, VEC, true, true, CT>(grid, block, stream, g, sc, out, C, ch0);
+    else if (cached) launch_box_kernel<CC, VEC, true, false, CT>(grid, block, stream, g, sc, out, C, ch0);
+    else if (mat) launch_box_kernel<CC, VEC, false, true, CT>(grid, block, stream, g, sc, out, C, ch0);
+    else launch_box_kernel<CC, VEC, false, false, CT>(grid, block, stream, g, sc, out, C, ch0);
     return cudaGetLastError();
 }
 
@@ -102,12 +139,12 @@ cudaError_t launch_box_filter(const DevGrid& g, const float* sidecar, int C, flo
         return cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, stream);
     }
     switch (C) {
-        case 1: return launch_box_cc<1, false>(g, sidecar, C, 0, out, resolver, output, stream);
-        case 2: return launch_box_cc<2, false>(g, sidecar, C, 0, out, resolver, output, stream);
-        case 3: return launch_box_cc<3, false>(g, sidecar, C, 0, out, resolver, output, stream);
-        case 4: return launch_box_cc<4, true>(g, sidecar, C, 0, out, resolver, output, stream);
-        case 8: return launch_box_cc<8, true>(g, sidecar, C, 0, out, resolver, output, stream);
-        case 16: return launch_box_cc<16, true>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 1: return launch_box_cc<1, false, 1>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 2: return launch_box_cc<2, false, 2>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 3: return launch_box_cc<3, false, 3>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 4: return launch_box_cc<4, true, 4>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 8: return launch_box_cc<8, true, 8>(g, sidecar, C, 0, out, resolver, output, stream);
+        case 16: return launch_box_cc<16, true, 16>(g, sidecar, C, 0, out, resolver, output, stream);
         default: break;
     }
     // Other widths: chunks of 4 channels (scalar loads), then the remainder.

@@ -20,9 +20,11 @@
 namespace vbm {
 namespace {
 
-template <int CC, bool VEC, bool CACHED, int OP>
+// CT > 0: the row stride C is the compile-time CT (and ch0 is 0).
+template <int CC, bool VEC, bool CACHED, int OP, int CT>
 __global__ void __launch_bounds__(512) cross_filter_kernel(DevGrid g, const float* __restrict__ sc,
-                                                           float* __restrict__ out, int C, int ch0) {
+                                                           float* __restrict__ out, int C_rt, int ch0_rt) {
+    const int C = CT > 0 ? CT : C_rt, ch0 = CT > 0 ? 0 : ch0_rt;
     __shared__ uint32_t table[CACHED ? VBM_MAX_CACHED_LEAVES * kCrossTaps : 1];
     const uint32_t W = 1u << g.log2w, words = W >> 6;
     const uint32_t b = blockIdx.x;
@@ -76,17 +78,17 @@ __global__ void __launch_bounds__(512) cross_taps_kernel(DevGrid g, uint32_t* __
     if (b == 0 && threadIdx.x < (unsigned)kCrossTaps) taps[threadIdx.x] = 0u;
 }
 
-template <int CC, bool VEC>
+template <int CC, bool VEC, int CT = 0>
 cudaError_t launch_cross_cc(const DevGrid& g, const float* sc, int C, int ch0, float* out, int resolver, int op,
                             cudaStream_t stream) {
     const dim3 grid(g.n_blocks), block(threads_for(g.log2w));
     const bool cached = resolver == VBM_RESOLVE_CACHED;
     if (op == VBM_CROSS_LAPLACIAN) {
-        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_LAPLACIAN><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
-        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_LAPLACIAN><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_LAPLACIAN, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_LAPLACIAN, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
     } else {
-        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_SUM><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
-        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_SUM><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        if (cached) cross_filter_kernel<CC, VEC, true, VBM_CROSS_SUM, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+        else cross_filter_kernel<CC, VEC, false, VBM_CROSS_SUM, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
     }
     return cudaGetLastError();
 }
@@ -97,12 +99,12 @@ cudaError_t launch_cross_filter(const DevGrid& g, const float* sidecar, int C, f
                                 cudaStream_t stream) {
     if (g.n_blocks == 0) return cudaMemsetAsync(out, 0, sizeof(float) * (size_t)C, stream);
     switch (C) {
-        case 1: return launch_cross_cc<1, false>(g, sidecar, C, 0, out, resolver, op, stream);
-        case 2: return launch_cross_cc<2, false>(g, sidecar, C, 0, out, resolver, op, stream);
-        case 3: return launch_cross_cc<3, false>(g, sidecar, C, 0, out, resolver, op, stream);
-        case 4: return launch_cross_cc<4, true>(g, sidecar, C, 0, out, resolver, op, stream);
-        case 8: return launch_cross_cc<8, true>(g, sidecar, C, 0, out, resolver, op, stream);
-        case 16: return launch_cross_cc<16, true>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 1: return launch_cross_cc<1, false, 1>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 2: return launch_cross_cc<2, false, 2>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 3: return launch_cross_cc<3, false, 3>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 4: return launch_cross_cc<4, true, 4>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 8: return launch_cross_cc<8, true, 8>(g, sidecar, C, 0, out, resolver, op, stream);
+        case 16: return launch_cross_cc<16, true, 16>(g, sidecar, C, 0, out, resolver, op, stream);
         default: break;
     }
     int ch0 = 0;

@@ -108,41 +108,26 @@ struct TapResolver {
     }
 };
 
-// The z-row of a leaf's mask word `word` (first index `base`: the word's entry
-// of the 9-bit directory pre-added to the leaf's first index) that starts at
-// bit yb (a multiple of 8): its 8 bits, and the index of the row's first
-// voxel.  A row lies in one 32-bit half of the word.
-struct RowByte {
-    uint32_t byte, rb;
-};
-__device__ __forceinline__ RowByte row_byte(uint64_t word, uint32_t base, uint32_t yb) {
-    const uint32_t lo = (uint32_t)word, hi = (uint32_t)(word >> 32);
-    const bool up = yb >= 32u;
-    const uint32_t half = up ? hi : lo, sh = yb & 31u;
-    RowByte r;
-    r.byte = (half >> sh) & 0xFFu;
-    r.rb = base + (up ? (uint32_t)__popc(lo) : 0u) + (uint32_t)__popc(half & ((1u << sh) - 1u));
-    return r;
-}
-
 // The three taps (di,dj,-1), (di,dj,0), (di,dj,+1) of a voxel at in-leaf
 // position (x,y,z), through its leaf's staged table row.  The three positions
-// lie in one z-row of one mask word of one leaf -- the word of x+di, the row of
-// y+dj -- so one popcount below bit z ranks all three (the z-1 bit, when set,
-// is one of the bits below z; the z+1 bit follows z), except where z-1 or z+1
-// crosses the leaf's z face (z = 0 or 7; never both): that tap is the last or
-// first bit of the same row of the z neighbour leaf.  Written without branches
-// (the z neighbour chosen by a select, its loads predicated), so that the loads
-// of all nine columns can be in flight together.
+// lie in one z-row (8 bits) of one mask word of one leaf -- the word of x+di,
+// the row of y+dj -- so one popcount of the word's bits below the centre ranks
+// all three (the z-1 bit, when set, is the last of those bits; the z+1 bit
+// follows the centre), except where z-1 or z+1 crosses the leaf's z face
+// (z = 0 or 7; never both): that tap is the last or first bit of the same row
+// of the z neighbour leaf.  The masks depend only on dj and z, so they are
+// shared by the three columns of a dj.  Written without branches (the z
+// neighbour chosen by a select, its loads predicated), so that the loads of all
+// nine columns can be in flight together.
 template <int DI, int DJ>
 __device__ __forceinline__ void cached_column(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ row,
                                               int32_t x, int32_t y, int32_t z, uint32_t (&idx)[3]) {
     const int32_t nx = x + DI, ny = y + DJ;
     const int32_t sxy = ((nx >> 3) + 1) * 9 + ((ny >> 3) + 1) * 3;
     const uint32_t w = (uint32_t)(nx & 7), yb = (uint32_t)(ny & 7) * 8u, zu = (uint32_t)z;
-    const uint32_t L0 = row[sxy + 1];
     const bool lo = zu == 0u, hi = zu == 7u;
-    const uint32_t Le = lo ? row[sxy] : hi ? row[sxy + 2] : kNone;
+    const uint32_t L0 = row[sxy + 1];
+    const uint32_t Le = (lo || hi) ? row[sxy + (lo ? 0 : 2)] : kNone;
     uint64_t word = 0, worde = 0;
     uint32_t base = 0, basee = 0;
     if (L0 != kNone) {
@@ -153,17 +138,16 @@ __device__ __forceinline__ void cached_column(const LeafRec* __restrict__ leaves
         worde = __ldg(&leaves[Le].mask[w]);
         basee = __ldg(&leaves[Le].base[w]);
     }
-    const RowByte r = row_byte(word, base, yb), e = row_byte(worde, basee, yb);
-    // bits z-1, z, z+1 of the row as bits 0, 1, 2 (0 past either end of the row)
-    const uint32_t b3 = ((r.byte << 1) >> zu) & 7u;
-    const uint32_t below = (uint32_t)__popc(r.byte & ((1u << zu) - 1u));
+    const uint32_t p = yb + zu;                         // the centre's bit, 0..63
+    const uint32_t pe = lo ? yb + 7u : yb;              // the face-crossing tap's bit in the z neighbour
+    const uint32_t cnt = (uint32_t)__popcll(word & ((1ull << p) - 1ull));
+    const uint32_t byte = (uint32_t)(word >> yb) & 0xFFu;
+    const uint32_t b3 = ((byte << 1) >> zu) & 7u;       // bits z-1, z, z+1 of the row (0 past its ends)
     const uint32_t bz = (b3 >> 1) & 1u;
-    // the face-crossing tap: the last bit of the -z neighbour's row, or the first of the +z one's
-    const uint32_t te = lo ? (((e.byte >> 7) & 1u) ? e.rb + (uint32_t)__popc(e.byte) - 1u : 0u)
-                           : ((e.byte & 1u) ? e.rb : 0u);
-    idx[1] = bz ? r.rb + below : 0u;
-    idx[0] = lo ? te : ((b3 & 1u) ? r.rb + below - 1u : 0u);
-    idx[2] = hi ? te : ((b3 & 4u) ? r.rb + below + bz : 0u);
+    const uint32_t te = ((worde >> pe) & 1ull) ? basee + (uint32_t)__popcll(worde & ((1ull << pe) - 1ull)) : 0u;
+    idx[1] = bz ? base + cnt : 0u;
+    idx[0] = lo ? te : ((b3 & 1u) ? base + cnt - 1u : 0u);
+    idx[2] = hi ? te : ((b3 & 4u) ? base + cnt + bz : 0u);
 }
 
 // The 27 box taps of one voxel in tap order, three at a time: column
