@@ -275,6 +275,8 @@ int vbm_box_filter_batch(const vbm_grid* grid, int count, const float* const* si
  *     asynchronous copies that overlap in both directions; pageable memory is
  *     accepted, and CUDA then copies synchronously with the calling thread.
  *   - Calls on one grid from several host threads are serialised by a lock.
+ *   - Unlike the device-buffer compute calls, this call is not for stream
+ *     capture: it may allocate, and it works on the grid's own streams.
  *   - No output may overlap a sidecar or another output (host byte ranges).
  * Errors: as vbm_box_filter_batch (INVALID for NULL host pointers), NOMEM
  * (staging allocation), CUDA. */
