@@ -335,6 +335,31 @@ def test_box_filter_batch_host_matches_oracle(resolver):
     g.close()
 
 
+def test_box_filter_batch_host_back_to_back():
+    """Five host-buffer calls enqueued back to back with no synchronisation
+    between them, each with its own pinned inputs and outputs: calls i and
+    i+2 reuse one staging set, so every output is correct only if each reuse
+    waits for the set's previous filter and copies back."""
+    t = gu.torch()
+    coords = SMALL["tiny_shell"]()
+    o = oracle.OracleGrid(coords)
+    g = vbm.vbm_build(coords, 9)
+    widths = (1, 3, 8, 16)
+    calls = []
+    for call in range(5):
+        hosts = [synth.sidecar_uniform(o.n, C, seed=1000 * call + C) for C in widths]
+        ins = [t.from_numpy(h).pin_memory() for h in hosts]
+        outs = [t.full((len(h),), float("nan")).pin_memory() for h in hosts]
+        vbm.vbm_box_filter_batch_host(g, ins, list(widths), outs, vbm.RESOLVE_BRICK)
+        calls.append((hosts, outs))
+    t.cuda.current_stream().synchronize()
+    for call, (hosts, outs) in enumerate(calls):
+        for h, C, out in zip(hosts, widths, outs):
+            np.testing.assert_array_equal(gu.bits(out.numpy()), gu.bits(o.box_filter(h, C)),
+                                          err_msg=f"call {call} C={C}")
+    g.close()
+
+
 def test_box_filter_batch_host_errors_and_empty_grid():
     t = gu.torch()
     g = vbm.vbm_build(SMALL["tiny_shell"](), 7)
