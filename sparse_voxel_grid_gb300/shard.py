@@ -91,10 +91,12 @@ def exchange_packed(plan: ShardPlan, sendbuf, C: int, group=None):
 class ShardedBoxFilter:
     """The box filter of this rank's blocks, with the halo exchanged first.
 
-    `run(sidecars, Cs, outs)`: sidecars are this rank's full-layout (N+1)*C
-    CUDA tensors with its own rows filled; the call fills their halo rows from
-    the other ranks, then writes this rank's output rows (and row 0 on rank 0)
-    of outs.  Collective: every rank of the group calls it with the same Cs."""
+    `run(sidecars, Cs, outs, stream)`: sidecars are this rank's full-layout
+    (N+1)*C CUDA tensors with its own rows filled; the call fills their halo
+    rows from the other ranks, then writes this rank's output rows (and row 0
+    on rank 0) of outs.  Collective: every rank of the group calls it with the
+    same Cs.  `stream`: None (torch's current stream) or a torch.cuda.Stream;
+    with gloo the exchange synchronises the device."""
 
     def __init__(self, grid, plan: ShardPlan, resolver=None, group=None):
         import torch
@@ -120,7 +122,14 @@ class ShardedBoxFilter:
             torch.cuda.synchronize()
             recv = exchange_packed(self.plan, sendbuf.cpu(), C, self.group).cuda()
             torch.cuda.synchronize()
+        elif isinstance(stream, torch.cuda.Stream):
+            # NCCL orders the collective after torch's current stream: make that
+            # the stream the gather ran on, so the scatter below sees the rows
+            with torch.cuda.stream(stream):
+                recv = exchange_packed(self.plan, sendbuf, C, self.group)
         else:
+            if stream is not None:
+                raise TypeError("with NCCL, stream must be None or a torch.cuda.Stream")
             recv = exchange_packed(self.plan, sendbuf, C, self.group)
         if len(self.recv_idx):
             check(lib.vbm_scatter_rows(ctypes.c_void_p(recv.data_ptr()), int(C),
