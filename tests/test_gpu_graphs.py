@@ -81,3 +81,41 @@ def test_two_streams_on_one_grid():
         vbm.vbm_box_filter(g, b, 8, ob, vbm.RESOLVE_BRICK, stream=s2)
     t.cuda.synchronize()
     assert t.equal(oa.view(t.int32), ra.view(t.int32)) and t.equal(ob.view(t.int32), rb.view(t.int32))
+
+
+def test_graph_capture_of_the_shard_calls():
+    """The block-range filter and the row gather/scatter are plain enqueues
+    too: a captured pack -> place -> filter of two block ranges replays to the
+    bits of the whole-grid call."""
+    import ctypes
+    t = gu.torch()
+    g = vbm.vbm_build(synth.WORKLOADS["T"](), 7)
+    n, C = g.n, 8
+    lib = vbm.load()
+    src = t.from_numpy(synth.sidecar_uniform(n, C, seed=9)).cuda()
+    want = t.empty_like(src)
+    vbm.vbm_box_filter(g, src, C, want, vbm.RESOLVE_BRICK)
+    rows = t.arange(1, n + 1, dtype=t.int32, device="cuda")  # every row: packed, then placed back
+    packed = t.empty(n * C, device="cuda")
+    side = t.full_like(src, float("nan"))
+    side[:C] = 0.0
+    out = t.full_like(src, float("nan"))
+    nb = g.info["n_blocks"]
+    t.cuda.synchronize()
+    P = ctypes.c_void_p
+    s = t.cuda.Stream()
+    graph = t.cuda.CUDAGraph()
+    with t.cuda.stream(s):
+        with t.cuda.graph(graph, stream=s):
+            h = P(s.cuda_stream)
+            assert lib.vbm_gather_rows(P(src.data_ptr()), C, P(rows.data_ptr()), n, P(packed.data_ptr()), h) == 0
+            assert lib.vbm_scatter_rows(P(packed.data_ptr()), C, P(rows.data_ptr()), n, P(side.data_ptr()), h) == 0
+            for b0, b1 in ((0, nb // 2), (nb // 2, nb)):
+                sc = (ctypes.c_void_p * 1)(side.data_ptr())
+                ou = (ctypes.c_void_p * 1)(out.data_ptr())
+                cs = (ctypes.c_int * 1)(C)
+                assert lib.vbm_box_filter_batch_blocks(g.handle, b0, b1, 1, sc, cs, ou, vbm.RESOLVE_BRICK, h) == 0
+    for _ in range(2):
+        graph.replay()
+    t.cuda.synchronize()
+    np.testing.assert_array_equal(gu.bits(out.cpu().numpy()), gu.bits(want.cpu().numpy()))
