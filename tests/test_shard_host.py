@@ -123,3 +123,39 @@ def test_halo_exchange_gloo(workload, log2w, world, C):
         assert p.exitcode == 0
     assert all(ok for ok, _ in got.values()), got
     assert all(nh > 0 for _, nh in got.values())
+
+
+def test_more_shards_than_blocks_and_empty_grids():
+    """Shards beyond the number of blocks are empty (no blocks, no halo) and
+    the non-empty ones still partition the indices; an empty grid gives empty
+    shards."""
+    coords = GRIDS["tiny_shell"]()
+    g = _host_grid(coords, 9)
+    nb = g.info["n_blocks"]
+    world = nb + 3
+    bb = shard.shard_blocks(g, world)
+    assert bb[0] == 0 and bb[-1] == nb
+    sizes = np.diff(bb.astype(np.int64))
+    assert (sizes >= 0).all() and sizes.sum() == nb and (sizes == 0).sum() == world - nb
+    for q in range(world):
+        h = shard.shard_halo(g, int(bb[q]), int(bb[q + 1]))
+        assert (len(h) == 0) == (sizes[q] == 0)
+    plan = shard.ShardPlan(g, world, world - 1)
+    assert sum(len(x) for x in plan.recv_rows) == len(plan.halo[world - 1])
+    e = _host_grid(np.zeros((0, 3), dtype=np.int32), 7)
+    assert (shard.shard_blocks(e, 4) == 0).all()
+    assert len(shard.shard_halo(e, 0, 0)) == 0
+
+
+def test_row_calls_validate_on_the_host():
+    """vbm_gather_rows / vbm_scatter_rows reject a bad channel count and
+    unaligned or NULL pointers before any CUDA call, and do nothing for a zero
+    count."""
+    import ctypes
+    lib = vbm.load()
+    P = ctypes.c_void_p
+    assert lib.vbm_gather_rows(P(16), 0, P(16), 1, P(16), None) == -1
+    assert lib.vbm_scatter_rows(P(16), 65, P(16), 1, P(16), None) == -1
+    assert lib.vbm_gather_rows(P(16), 1, P(16), 0, P(16), None) == 0  # nothing to move
+    assert lib.vbm_gather_rows(None, 1, P(16), 1, P(16), None) == -1
+    assert lib.vbm_scatter_rows(P(18), 1, P(16), 1, P(16), None) == -6
