@@ -32,23 +32,22 @@ __device__ __forceinline__ void box_filter_block(const DevGrid& g, const float* 
     const uint32_t b = g.block0 + blockIdx.x;
     const uint64_t* jb = g.jump + (size_t)b * words;
     const uint32_t fl = __ldg(&g.first_leaf[b]);
+    // One slot per thread (blockDim == W).  The slot is decoded before the
+    // cached table is staged: the decode's loads do not depend on the table,
+    // so they are in flight while the staging's are.
+    const uint32_t s = threadIdx.x, index = 1u + b * W + s;
+    const bool valid = s < W && index <= g.n;
+    Slot d{0u, 0u};
+    if (valid) d = decode_slot(g, fl, jb, s, index);
     bool use_table = false;
     if constexpr (CACHED) {
         const uint32_t span = block_span(jb, words);
         use_table = span <= VBM_MAX_CACHED_LEAVES;  // block-uniform: the barrier inside is safe
         if (use_table) stage_leaf_table(g, fl, span, table);
     }
-    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
-        const uint32_t index = 1u + b * W + s;
-        if (index > g.n) break;
-        const Slot d = decode_slot(g, fl, jb, s, index);
-        if constexpr (CACHED) {
-            if (use_table) {
-                box_slot<CC, VEC, true, MAT>(g, table + (d.leaf - fl) * kBoxTaps, d, index, sc, out, C, ch0);
-                continue;
-            }
-        }
-        box_slot<CC, VEC, false, MAT>(g, nullptr, d, index, sc, out, C, ch0);
+    if (valid) {
+        if (CACHED && use_table) box_slot<CC, VEC, true, MAT>(g, table + (d.leaf - fl) * kBoxTaps, d, index, sc, out, C, ch0);
+        else box_slot<CC, VEC, false, MAT>(g, nullptr, d, index, sc, out, C, ch0);
     }
     if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
 }

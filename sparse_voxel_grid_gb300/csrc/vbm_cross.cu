@@ -30,23 +30,21 @@ __global__ void __launch_bounds__(512) cross_filter_kernel(DevGrid g, const floa
     const uint32_t b = blockIdx.x;
     const uint64_t* jb = g.jump + (size_t)b * words;
     const uint32_t fl = __ldg(&g.first_leaf[b]);
+    // One slot per thread (blockDim == W), decoded before the cached table is
+    // staged so that the two sets of loads are in flight together.
+    const uint32_t s = threadIdx.x, index = 1u + b * W + s;
+    const bool valid = s < W && index <= g.n;
+    Slot d{0u, 0u};
+    if (valid) d = decode_slot(g, fl, jb, s, index);
     bool use_table = false;
     if constexpr (CACHED) {
         const uint32_t span = block_span(jb, words);
         use_table = span <= VBM_MAX_CACHED_LEAVES;
         if (use_table) stage_cross_table(g, fl, span, table);
     }
-    for (uint32_t s = threadIdx.x; s < W; s += blockDim.x) {
-        const uint32_t index = 1u + b * W + s;
-        if (index > g.n) break;
-        const Slot d = decode_slot(g, fl, jb, s, index);
-        if constexpr (CACHED) {
-            if (use_table) {
-                cross_slot<CC, VEC, true, OP>(g, table + (d.leaf - fl) * kCrossTaps, d, index, sc, out, C, ch0);
-                continue;
-            }
-        }
-        cross_slot<CC, VEC, false, OP>(g, nullptr, d, index, sc, out, C, ch0);
+    if (valid) {
+        if (CACHED && use_table) cross_slot<CC, VEC, true, OP>(g, table + (d.leaf - fl) * kCrossTaps, d, index, sc, out, C, ch0);
+        else cross_slot<CC, VEC, false, OP>(g, nullptr, d, index, sc, out, C, ch0);
     }
     if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
 }
