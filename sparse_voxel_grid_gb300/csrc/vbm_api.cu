@@ -60,7 +60,7 @@ class DeviceGuard {
 int upload(vbm_grid* g, cudaStream_t stream) {
     const vbm::ArenaLayout lay = vbm::arena_layout(g->leaves.size(), g->root_keys.size(), g->n_lower,
                                                    g->first_leaf.size(), g->log2w);
-    const void* src[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
+    const void* src[vbm::kHostArrays] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
                           g->first_leaf.data(), g->jump.data(), g->nbr.data()};
     cudaError_t e = cudaGetDevice(&g->device);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaGetDevice", e);
@@ -76,11 +76,14 @@ int upload(vbm_grid* g, cudaStream_t stream) {
     }
     g->arena_bytes = lay.total;
     char* base = static_cast<char*>(g->arena);
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < vbm::kHostArrays; ++i) {
         if (!lay.bytes[i]) continue;
         e = cudaMemcpyAsync(base + lay.off[i], src[i], lay.bytes[i], cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return fail_cuda("vbm_build: cudaMemcpyAsync", e);
     }
+    e = vbm::launch_row_ranks(reinterpret_cast<const vbm::LeafRec*>(base + lay.off[0]), (uint32_t)g->leaves.size(),
+                              reinterpret_cast<uint2*>(base + lay.off[7]), stream);
+    if (e != cudaSuccess) return fail_cuda("vbm_build: row ranks", e);
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);
     vbm::set_device_views(g, lay, sm_count);
@@ -107,12 +110,12 @@ int fill_mirrors(const vbm_grid* cg) {
     } catch (const std::bad_alloc&) {
         return fail(VBM_ERR_NOMEM, "vbm_leaf_export: out of host memory");
     }
-    void* dst[7] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
+    void* dst[vbm::kHostArrays] = {g->leaves.data(), g->root_keys.data(), g->upper.data(), g->lower.data(),
                     g->first_leaf.data(), g->jump.data(), g->nbr.data()};
     DeviceGuard guard(g->device);
     if (!guard.ok()) return fail(VBM_ERR_CUDA, "vbm_leaf_export: cannot select the grid's device");
     const char* base = static_cast<const char*>(g->arena);
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < vbm::kHostArrays; ++i) {
         if (!lay.bytes[i]) continue;
         const cudaError_t e = cudaMemcpy(dst[i], base + lay.off[i], lay.bytes[i], cudaMemcpyDeviceToHost);
         if (e != cudaSuccess) return fail_cuda("vbm_leaf_export: cudaMemcpy", e);

@@ -68,6 +68,12 @@ __global__ void __launch_bounds__(512, 3) box_filter_kernel_r40(DevGrid g, const
     box_filter_block<CC, VEC, CACHED, MAT, CT>(g, sc, out, C, ch0);
 }
 
+template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
+__global__ void __launch_bounds__(512, 4) box_filter_kernel_r32(DevGrid g, const float* __restrict__ sc,
+                                                                float* __restrict__ out, int C, int ch0) {
+    box_filter_block<CC, VEC, CACHED, MAT, CT>(g, sc, out, C, ch0);
+}
+
 // The materialised forms are held to 64 registers (2 CTAs of 512 threads per
 // SM): with a compile-time stride the C=16 ones otherwise take 78-82 and run
 // 11-28% slower.
@@ -81,6 +87,7 @@ template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
 void launch_box_kernel(dim3 grid, dim3 block, cudaStream_t stream, const DevGrid& g, const float* sc, float* out,
                        int C, int ch0) {
     if constexpr (MAT) box_filter_kernel_r64<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
+    else if constexpr (CC <= 3 && CACHED) box_filter_kernel_r32<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
     else if constexpr (CC <= 3) box_filter_kernel_r40<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
     else box_filter_kernel<CC, VEC, CACHED, MAT, CT><<<grid, block, 0, stream>>>(g, sc, out, C, ch0);
 }

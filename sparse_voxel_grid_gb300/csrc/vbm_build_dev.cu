@@ -264,6 +264,18 @@ __global__ void nbr_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, uint
 }
 
 // 5e. Spans: max and the number of blocks over MaxCachedLeaves.
+// Row ranks (kRowRanks): one (leaf, row) entry per thread, grid-stride.
+__global__ void rowrank_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, uint2* __restrict__ rowrank) {
+    const uint64_t total = (uint64_t)nl * kRowRanks, stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
+        const LeafRec& r = leaves[e >> 6];
+        const uint32_t x = (uint32_t)(e >> 3) & 7u, shift = 8u * ((uint32_t)e & 7u);
+        const uint64_t word = r.mask[x];
+        rowrank[e] = make_uint2(r.base[x] + (uint32_t)__popcll(word & ((1ull << shift) - 1ull)),
+                                (uint32_t)(word >> shift) & 0xFFu);
+    }
+}
+
 __global__ void span_kernel(const unsigned long long* __restrict__ jump, uint32_t n_blocks, uint32_t words,
                             uint32_t* __restrict__ out) {
     for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < n_blocks; b += gridDim.x * blockDim.x) {
@@ -493,6 +505,8 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
         blocks_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(leaves, nl, log2w, first_leaf, jump);
         nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
                                                                                  final_of, nbr);
+        rowrank_kernel<<<grid_for((uint64_t)nl * kRowRanks, sm), kThreads, 0, st>>>(
+            leaves, nl, reinterpret_cast<uint2*>(base + lay.off[7]));
         span_kernel<<<grid_for(g->n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)g->n_blocks, words, ctr + 3);
         VBM_CK(cudaGetLastError());
     }
@@ -698,6 +712,8 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
         blocks_kernel<<<grid_for(nl, sm), kThreads, 0, st>>>(leaves, nl, log2w, first_leaf, jump);
         nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
                                                                                  final_of, nbr);
+        rowrank_kernel<<<grid_for((uint64_t)nl * kRowRanks, sm), kThreads, 0, st>>>(
+            leaves, nl, reinterpret_cast<uint2*>(base + lay.off[7]));
         span_kernel<<<grid_for(n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)n_blocks, words, ctr + 3);
         VBM_CK(cudaGetLastError());
     }
@@ -709,6 +725,16 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
     VBM_CK(prepare_device_kernels(device));
 #undef VBM_CK
     return VBM_OK;
+}
+
+cudaError_t launch_row_ranks(const LeafRec* leaves, uint32_t n_leaves, uint2* rowrank, cudaStream_t stream) {
+    if (!n_leaves) return cudaSuccess;
+    int device = 0, sm = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    rowrank_kernel<<<grid_for((uint64_t)n_leaves * kRowRanks, sm), kThreads, 0, stream>>>(leaves, n_leaves, rowrank);
+    return cudaGetLastError();
 }
 
 }  // namespace vbm

@@ -94,6 +94,15 @@ __device__ __forceinline__ uint32_t leaf_index_at(const LeafRec* __restrict__ le
     return __ldg(&r->base[w]) + (uint32_t)__popcll(word & ((1ull << bit) - 1ull));
 }
 
+// The same through the leaf's row ranks (kRowRanks): entry off>>3 is the z-row
+// (x, y) of off = x*64 + y*8 + z; one 8-byte load and a popcount of the row's
+// bits below z.
+__device__ __forceinline__ uint32_t row_index_at(const uint2* __restrict__ rowrank, uint32_t L, uint32_t off) {
+    const uint2 e = __ldg(&rowrank[(size_t)L * kRowRanks + (off >> 3)]);
+    const uint32_t z = off & 7u;
+    return ((e.y >> z) & 1u) ? e.x + (uint32_t)__popc(e.y & ((1u << z) - 1u)) : 0u;
+}
+
 __device__ __forceinline__ uint32_t pack_off(int32_t x, int32_t y, int32_t z) {
     return (uint32_t)((x & 7) << 6 | (y & 7) << 3 | (z & 7));
 }
@@ -123,7 +132,7 @@ __device__ __forceinline__ uint32_t find_leaf(const DevGrid& g, int32_t x, int32
 // Index of the voxel at (x,y,z), 0 if inactive, by tree walk.
 __device__ __forceinline__ uint32_t walk_index(const DevGrid& g, int32_t x, int32_t y, int32_t z) {
     const uint32_t L = find_leaf(g, x, y, z);
-    return L == kNone ? 0u : leaf_index_at(g.leaves, L, pack_off(x, y, z));
+    return L == kNone ? 0u : row_index_at(g.rowrank, L, pack_off(x, y, z));
 }
 
 // ---------------------------------------------------------------------------
@@ -150,11 +159,11 @@ __device__ __forceinline__ void stage_leaf_table(const DevGrid& g, uint32_t firs
 // Index of the in-leaf-relative position (nx,ny,nz), each in -1..8, of a voxel
 // of table row `row` (the voxel's leaf is firstLeafID + row): which of the 27
 // neighbour leaves holds it follows from floor(n/8), then an in-leaf rank.
-__device__ __forceinline__ uint32_t cached_index(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ row,
+__device__ __forceinline__ uint32_t cached_index(const uint2* __restrict__ rowrank, const uint32_t* __restrict__ row,
                                                  int32_t nx, int32_t ny, int32_t nz) {
     const int32_t slot = ((nx >> 3) + 1) * 9 + ((ny >> 3) + 1) * 3 + ((nz >> 3) + 1);
     const uint32_t NL = row[slot];
-    return NL == kNone ? 0u : leaf_index_at(leaves, NL, pack_off(nx, ny, nz));
+    return NL == kNone ? 0u : row_index_at(rowrank, NL, pack_off(nx, ny, nz));
 }
 
 // Number of leaves the block spans: 1 + popcount(jumpMap).

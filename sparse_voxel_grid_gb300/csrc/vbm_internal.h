@@ -9,6 +9,8 @@
 #include <string>
 #include <vector>
 
+#include <vector_types.h>
+
 #include "../../include/vbm.h"
 
 #ifdef __CUDACC__
@@ -28,6 +30,12 @@ constexpr int kCrossTaps = 7;
 constexpr int kWenoTaps = 19;
 constexpr int kMaxC = 64;
 constexpr int kNbrStride = 32;              // neighbour-row stride: 27 ids + 5 pad = one 128-byte line
+// Row ranks: entry L*64 + x*8 + y describes the z-row (x, y, 0..7) of leaf L:
+// .y = its 8 mask bits (bit z = voxel (x,y,z) active), .x = the index the
+// row's first active voxel has or would have (the leaf's first index plus the
+// active voxels before the row in leaf order).  A finer copy of the leaf's
+// rank directory, derived from the masks on the device after every build.
+constexpr int kRowRanks = 64;
 
 // One leaf: 128 bytes, one cache line.  `mask` is the 512-bit value mask (bit
 // off%64 of word off/64, off = x*64 + y*8 + z in-leaf); `prefix` is the 9-bit
@@ -63,6 +71,7 @@ struct DevGrid {
     const uint32_t* first_leaf;  // n_blocks
     const uint64_t* jump;        // n_blocks x (W/64)
     const uint32_t* nbr;         // n_leaves x kNbrStride: neighbour-leaf ids (see vbm_build.cpp)
+    const uint2* rowrank;        // n_leaves x 64: row ranks of each leaf (see kRowRanks)
     uint32_t n;                  // active voxels
     uint32_t n_leaves;
     uint32_t n_blocks;           // blocks a launch covers (CTAs of a one-CTA-per-block kernel)
@@ -113,10 +122,12 @@ struct vbm_grid {
 namespace vbm {
 
 // Byte offsets of the grid's arrays in its one device allocation, in the order
-// leaves, root_keys, upper, lower, first_leaf, jump, nbr (256-byte aligned).
+// leaves, root_keys, upper, lower, first_leaf, jump, nbr, rowrank (256-byte
+// aligned).  The first seven have host copies; rowrank is made on the device.
+constexpr int kArenaArrays = 8, kHostArrays = 7;
 struct ArenaLayout {
-    size_t off[7];
-    size_t bytes[7];
+    size_t off[kArenaArrays];
+    size_t bytes[kArenaArrays];
     size_t total;
 };
 
@@ -130,8 +141,9 @@ inline ArenaLayout arena_layout(size_t n_leaves, size_t n_upper, size_t n_lower,
     a.bytes[4] = n_blocks * sizeof(uint32_t);
     a.bytes[5] = n_blocks * words * sizeof(uint64_t);
     a.bytes[6] = n_leaves * (size_t)kNbrStride * sizeof(uint32_t);
+    a.bytes[7] = n_leaves * (size_t)kRowRanks * 2 * sizeof(uint32_t);
     size_t total = 0;
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < kArenaArrays; ++i) {
         a.off[i] = total;
         total = (total + a.bytes[i] + 255) / 256 * 256;
     }
@@ -150,6 +162,7 @@ inline void set_device_views(vbm_grid* g, const ArenaLayout& a, int sm_count) {
     d.first_leaf = reinterpret_cast<const uint32_t*>(base + a.off[4]);
     d.jump = reinterpret_cast<const uint64_t*>(base + a.off[5]);
     d.nbr = reinterpret_cast<const uint32_t*>(base + a.off[6]);
+    d.rowrank = reinterpret_cast<const uint2*>(base + a.off[7]);
     d.n = (uint32_t)g->n;
     d.n_leaves = (uint32_t)g->n_leaves;
     d.n_blocks = (uint32_t)g->n_blocks;

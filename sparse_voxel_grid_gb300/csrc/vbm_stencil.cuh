@@ -103,51 +103,43 @@ struct TapResolver {
         }
     }
     __device__ __forceinline__ uint32_t operator()(int di, int dj, int dk) const {
-        if constexpr (TABLE) return cached_index(g->leaves, row, x + di, y + dj, z + dk);
+        if constexpr (TABLE) return cached_index(g->rowrank, row, x + di, y + dj, z + dk);
         else return walk_index(*g, x + di, y + dj, z + dk);
     }
 };
 
 // The three taps (di,dj,-1), (di,dj,0), (di,dj,+1) of a voxel at in-leaf
 // position (x,y,z), through its leaf's staged table row.  The three positions
-// lie in one z-row (8 bits) of one mask word of one leaf -- the word of x+di,
-// the row of y+dj -- so one popcount of the word's bits below the centre ranks
-// all three (the z-1 bit, when set, is the last of those bits; the z+1 bit
-// follows the centre), except where z-1 or z+1 crosses the leaf's z face
-// (z = 0 or 7; never both): that tap is the last or first bit of the same row
-// of the z neighbour leaf.  The masks depend only on dj and z, so they are
-// shared by the three columns of a dj.  Written without branches (the z
-// neighbour chosen by a select, its loads predicated), so that the loads of all
-// nine columns can be in flight together.
+// lie in one z-row of one leaf -- the row (x+di, y+dj) -- so that row's rank
+// entry (kRowRanks: its 8 mask bits and the index of its first bit) and one
+// popcount of its bits below z rank all three (the z-1 bit, when set, is the
+// last of those bits; the z+1 bit follows the centre), except where z-1 or z+1
+// crosses the leaf's z face (z = 0 or 7; never both): that tap is the last or
+// first bit of the same row of the z neighbour leaf.  Written without branches
+// (the z neighbour chosen by a select, its load predicated), so that the loads
+// of all nine columns can be in flight together.
 template <int DI, int DJ>
-__device__ __forceinline__ void cached_column(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ row,
+__device__ __forceinline__ void cached_column(const uint2* __restrict__ rowrank, const uint32_t* __restrict__ row,
                                               int32_t x, int32_t y, int32_t z, uint32_t (&idx)[3]) {
     const int32_t nx = x + DI, ny = y + DJ;
     const int32_t sxy = ((nx >> 3) + 1) * 9 + ((ny >> 3) + 1) * 3;
-    const uint32_t w = (uint32_t)(nx & 7), yb = (uint32_t)(ny & 7) * 8u, zu = (uint32_t)z;
+    const uint32_t r = (uint32_t)(nx & 7) * 8u + (uint32_t)(ny & 7), zu = (uint32_t)z;
     const bool lo = zu == 0u, hi = zu == 7u;
     const uint32_t L0 = row[sxy + 1];
     const uint32_t Le = (lo || hi) ? row[sxy + (lo ? 0 : 2)] : kNone;
-    uint64_t word = 0, worde = 0;
-    uint32_t base = 0, basee = 0;
-    if (L0 != kNone) {
-        word = __ldg(&leaves[L0].mask[w]);
-        base = __ldg(&leaves[L0].base[w]);
-    }
-    if (Le != kNone) {
-        worde = __ldg(&leaves[Le].mask[w]);
-        basee = __ldg(&leaves[Le].base[w]);
-    }
-    const uint32_t p = yb + zu;                         // the centre's bit, 0..63
-    const uint32_t pe = lo ? yb + 7u : yb;              // the face-crossing tap's bit in the z neighbour
-    const uint32_t cnt = (uint32_t)__popcll(word & ((1ull << p) - 1ull));
-    const uint32_t byte = (uint32_t)(word >> yb) & 0xFFu;
-    const uint32_t b3 = ((byte << 1) >> zu) & 7u;       // bits z-1, z, z+1 of the row (0 past its ends)
+    uint2 c = make_uint2(0u, 0u), e = make_uint2(0u, 0u);
+    if (L0 != kNone) c = __ldg(&rowrank[(size_t)L0 * kRowRanks + r]);
+    if (Le != kNone) e = __ldg(&rowrank[(size_t)Le * kRowRanks + r]);
+    const uint32_t cnt = (uint32_t)__popc(c.y & ((1u << zu) - 1u));  // row bits below the centre
+    const uint32_t b3 = ((c.y << 1) >> zu) & 7u;                    // bits z-1, z, z+1 (0 past the row's ends)
     const uint32_t bz = (b3 >> 1) & 1u;
-    const uint32_t te = ((worde >> pe) & 1ull) ? basee + (uint32_t)__popcll(worde & ((1ull << pe) - 1ull)) : 0u;
-    idx[1] = bz ? base + cnt : 0u;
-    idx[0] = lo ? te : ((b3 & 1u) ? base + cnt - 1u : 0u);
-    idx[2] = hi ? te : ((b3 & 4u) ? base + cnt + bz : 0u);
+    // Face-crossing tap: bit 7 of the -z neighbour's row (after its bits 0..6),
+    // or bit 0 of the +z neighbour's row.
+    const uint32_t te = lo ? (((e.y >> 7) & 1u) ? e.x + (uint32_t)__popc(e.y & 0x7Fu) : 0u)
+                           : ((e.y & 1u) ? e.x : 0u);
+    idx[1] = bz ? c.x + cnt : 0u;
+    idx[0] = lo ? te : ((b3 & 1u) ? c.x + cnt - 1u : 0u);
+    idx[2] = hi ? te : ((b3 & 4u) ? c.x + cnt + bz : 0u);
 }
 
 // The 27 box taps of one voxel in tap order, three at a time: column
@@ -155,7 +147,7 @@ __device__ __forceinline__ void cached_column(const LeafRec* __restrict__ leaves
 template <int C3>
 __device__ __forceinline__ void box_column(const DevGrid& g, const uint32_t* table_row, int32_t x, int32_t y,
                                            int32_t z, uint32_t (&idx)[3]) {
-    cached_column<C3 / 3 - 1, C3 % 3 - 1>(g.leaves, table_row, x, y, z, idx);
+    cached_column<C3 / 3 - 1, C3 % 3 - 1>(g.rowrank, table_row, x, y, z, idx);
 }
 
 // 27-tap box filter of one voxel ([2262] "What changed"): taps in order
@@ -242,7 +234,7 @@ __device__ __forceinline__ void resolve_cross(const DevGrid& g, const uint32_t* 
             const int32_t nx = lx + cross_di(j), ny = ly + cross_dj(j), nz = lz + cross_dk(j);
             const bool leaves_leaf = ((nx | ny | nz) & ~7) != 0;  // some coordinate is -1 or 8
             const uint32_t NL = table_row[leaves_leaf ? j : 3];
-            st[j] = NL == kNone ? 0u : leaf_index_at(g.leaves, NL, pack_off(nx, ny, nz));
+            st[j] = NL == kNone ? 0u : row_index_at(g.rowrank, NL, pack_off(nx, ny, nz));
         }
     } else {
         const LeafRec* r = g.leaves + d.leaf;

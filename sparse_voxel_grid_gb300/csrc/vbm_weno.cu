@@ -32,7 +32,7 @@ __device__ __forceinline__ uint32_t weno_tap(const DevGrid& g, const uint32_t* r
         uint32_t NL = leaf;
         if (n < 0) NL = row[a];
         else if (n > 7) NL = row[6 - a];
-        return NL == kNone ? 0u : leaf_index_at(g.leaves, NL, pack_off(nx, ny, nz));
+        return NL == kNone ? 0u : row_index_at(g.rowrank, NL, pack_off(nx, ny, nz));
     } else {
         (void)row;
         (void)leaf;
