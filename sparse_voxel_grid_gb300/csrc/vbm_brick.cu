@@ -70,23 +70,44 @@ __host__ __device__ constexpr size_t brick_smem_bytes(int log2w) {
 // The 10 indices of brick row (bx, by) of the leaf whose neighbour row is
 // `nrow` (27 leaf ids at (dx+1)*9 + (dy+1)*3 + (dz+1)).  Cell k holds
 // leaf-relative z = k-1: cells 1..8 from the leaf at (dx,dy,0), cell 0 from
-// (dx,dy,-1) (its z = 7) and cell 9 from (dx,dy,+1) (its z = 0).
-__device__ __forceinline__ void brick_row(const uint2* __restrict__ rowrank, const uint32_t* __restrict__ nrow, int bx,
-                                          int by, uint32_t (&idx)[kEdge]) {
-    const int rx = bx - 1, ry = by - 1;                                  // -1..8
-    const int sx = (rx >> 3) + 1, sy = (ry >> 3) + 1;                    // 0..2
-    const uint32_t rr = (uint32_t)(rx & 7) * 8u + (uint32_t)(ry & 7);    // the z-row's rank entry (kRowRanks)
+// (dx,dy,-1) (its z = 7) and cell 9 from (dx,dy,+1) (its z = 0).  RR: ranked
+// from the three leaves' row-rank entries of the z-row (kRowRanks); otherwise
+// from their mask words and pre-added bases in the leaf records, which the
+// decode has just read for the block's own leaves.
+template <bool RR>
+__device__ __forceinline__ void brick_row(const DevGrid& g, const uint32_t* __restrict__ nrow, int bx, int by,
+                                          uint32_t (&idx)[kEdge]) {
+    const int rx = bx - 1, ry = by - 1;                // -1..8
+    const int sx = (rx >> 3) + 1, sy = (ry >> 3) + 1;  // 0..2
     const uint32_t* col = nrow + sx * 9 + sy * 3;
     const uint32_t Lm = __ldg(col), L0 = __ldg(col + 1), Lp = __ldg(col + 2);
-    uint2 c = make_uint2(0u, 0u), m = make_uint2(0u, 0u), p = make_uint2(0u, 0u);
-    if (L0 != kNone) c = __ldg(&rowrank[(size_t)L0 * kRowRanks + rr]);
-    if (Lm != kNone) m = __ldg(&rowrank[(size_t)Lm * kRowRanks + rr]);
-    if (Lp != kNone) p = __ldg(&rowrank[(size_t)Lp * kRowRanks + rr]);
+    if constexpr (RR) {
+        const uint32_t rr = (uint32_t)(rx & 7) * 8u + (uint32_t)(ry & 7);  // the z-row's entry
+        uint2 c = make_uint2(0u, 0u), m = make_uint2(0u, 0u), p = make_uint2(0u, 0u);
+        if (L0 != kNone) c = __ldg(&g.rowrank[(size_t)L0 * kRowRanks + rr]);
+        if (Lm != kNone) m = __ldg(&g.rowrank[(size_t)Lm * kRowRanks + rr]);
+        if (Lp != kNone) p = __ldg(&g.rowrank[(size_t)Lp * kRowRanks + rr]);
 #pragma unroll
-    for (int z = 0; z < 8; ++z)
-        idx[1 + z] = ((c.y >> z) & 1u) ? c.x + (uint32_t)__popc(c.y & ((1u << z) - 1u)) : 0u;
-    idx[0] = ((m.y >> 7) & 1u) ? m.x + (uint32_t)__popc(m.y & 0x7Fu) : 0u;  // z = 7 of the -z neighbour
-    idx[kEdge - 1] = (p.y & 1u) ? p.x : 0u;                                // z = 0 of the +z neighbour
+        for (int z = 0; z < 8; ++z)
+            idx[1 + z] = ((c.y >> z) & 1u) ? c.x + (uint32_t)__popc(c.y & ((1u << z) - 1u)) : 0u;
+        idx[0] = ((m.y >> 7) & 1u) ? m.x + (uint32_t)__popc(m.y & 0x7Fu) : 0u;  // z = 7 of the -z neighbour
+        idx[kEdge - 1] = (p.y & 1u) ? p.x : 0u;                                // z = 0 of the +z neighbour
+    } else {
+        const uint32_t xw = (uint32_t)(rx & 7);       // mask word of plane x
+        const uint32_t yb = (uint32_t)(ry & 7) * 8u;  // first bit of the z-row
+        uint32_t byte = 0, rb = 0;
+        if (L0 != kNone) {
+            const LeafRec* r = g.leaves + L0;
+            const uint64_t word = __ldg(&r->mask[xw]);
+            byte = (uint32_t)(word >> yb) & 0xFFu;
+            rb = __ldg(&r->base[xw]) + (uint32_t)__popcll(word & ((1ull << yb) - 1ull));
+        }
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+            idx[1 + z] = ((byte >> z) & 1u) ? rb + (uint32_t)__popc(byte & ((1u << z) - 1u)) : 0u;
+        idx[0] = Lm != kNone ? leaf_index_at(g.leaves, Lm, xw * 64u + yb + 7u) : 0u;
+        idx[kEdge - 1] = Lp != kNone ? leaf_index_at(g.leaves, Lp, xw * 64u + yb) : 0u;
+    }
 }
 
 // Brick cell of a voxel's own position (its (0,0,0) tap).
@@ -103,7 +124,7 @@ __device__ __forceinline__ constexpr int cross_cell_delta(int j) { return cross_
 // i.e. brick planes [x(first), x(last)+3).  One row per thread.  VALUES (one
 // channel only): store sidecar[idx] (+0.0 where idx == 0) instead of idx.
 // Ends with a barrier.
-template <bool VALUES>
+template <bool VALUES, bool RR = VALUES>
 __device__ __forceinline__ void build_round(const DevGrid& g, const BrickCtx& k, const uint16_t* offs,
                                             const uint16_t* starts, uint32_t l0, uint32_t nb, uint32_t* ib,
                                             const float* __restrict__ sc) {
@@ -112,7 +133,7 @@ __device__ __forceinline__ void build_round(const DevGrid& g, const BrickCtx& k,
         const uint32_t x0 = offs[starts[l]] >> 6, x1 = (offs[starts[l + 1] - 1u] >> 6) + 3u;
         if (row < x0 * 10u || row >= x1 * 10u) continue;
         uint32_t idx[kEdge];
-        brick_row(g.rowrank, g.nbr + (size_t)(k.fl + l) * kNbrStride, (int)(row / 10u), (int)(row % 10u), idx);
+        brick_row<RR>(g, g.nbr + (size_t)(k.fl + l) * kNbrStride, (int)(row / 10u), (int)(row % 10u), idx);
         uint32_t* dst = ib + kk * kCells + row * kEdge;
         if constexpr (VALUES) {
             float v[kEdge];
@@ -398,7 +419,7 @@ __global__ void __launch_bounds__(512, 3) brick_box_shared_kernel(
     brick_prologue<false>(g, k, m.offs, m.lof, m.starts, g.block0 + blockIdx.x);
     for (uint32_t l0 = 0; l0 < k.span; l0 += m.group) {
         const uint32_t nb = min(m.group, k.span - l0);
-        build_round<false>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
+        build_round<false, true>(g, k, m.offs, m.starts, l0, nb, m.ib, nullptr);
         const uint32_t sb = m.starts[l0], se = m.starts[l0 + nb];
         if (a.pair[0]) {
             gather_pair_entry<0>(k, m, l0, sb, se, a, s0, o0, s1, o1);

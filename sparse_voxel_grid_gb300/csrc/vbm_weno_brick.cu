@@ -62,12 +62,18 @@ __device__ __forceinline__ void weno_row_xy(uint32_t r, int& x, int& y) {
 }
 
 // Indices of leaf L's cells (x&7, y&7, 0..7) (0 where inactive or L is kNone).
-__device__ __forceinline__ void row_indices8(const uint2* __restrict__ rowrank, uint32_t L, int x, int y,
+__device__ __forceinline__ void row_indices8(const LeafRec* __restrict__ leaves, uint32_t L, int x, int y,
                                              uint32_t (&idx)[8]) {
-    uint2 e = make_uint2(0u, 0u);
-    if (L != kNone) e = __ldg(&rowrank[(size_t)L * kRowRanks + (uint32_t)(x & 7) * 8u + (uint32_t)(y & 7)]);
+    uint32_t byte = 0, rb = 0;
+    if (L != kNone) {
+        const LeafRec* r = leaves + L;
+        const uint32_t xw = (uint32_t)(x & 7), yb = (uint32_t)(y & 7) * 8u;
+        const uint64_t word = __ldg(&r->mask[xw]);
+        byte = (uint32_t)(word >> yb) & 0xFFu;
+        rb = __ldg(&r->base[xw]) + (uint32_t)__popcll(word & ((1ull << yb) - 1ull));
+    }
 #pragma unroll
-    for (int z = 0; z < 8; ++z) idx[z] = ((e.y >> z) & 1u) ? e.x + (uint32_t)__popc(e.y & ((1u << z) - 1u)) : 0u;
+    for (int z = 0; z < 8; ++z) idx[z] = ((byte >> z) & 1u) ? rb + (uint32_t)__popc(byte & ((1u << z) - 1u)) : 0u;
 }
 
 template <bool VALUES>
@@ -83,7 +89,7 @@ __device__ __forceinline__ void weno_build_round(const DevGrid& g, const BrickCt
         const uint32_t* nrow = g.nbr + (size_t)(k.fl + l) * kNbrStride;
         const int sx = x < 0 ? 0 : x > 7 ? 2 : 1, sy = y < 0 ? 0 : y > 7 ? 2 : 1;
         uint32_t idx[8];
-        row_indices8(g.rowrank, __ldg(nrow + sx * 9 + sy * 3 + 1), x, y, idx);
+        row_indices8(g.leaves, __ldg(nrow + sx * 9 + sy * 3 + 1), x, y, idx);
         uint32_t* dst = wb + kk * kWCells + wcell(x, y, 0);
         if constexpr (VALUES) {
 #pragma unroll
@@ -94,8 +100,8 @@ __device__ __forceinline__ void weno_build_round(const DevGrid& g, const BrickCt
         }
         if (r < 64u) {  // core row: the z halo, 3 cells from each z neighbour
             uint32_t lo[8], hi[8];
-            row_indices8(g.rowrank, __ldg(nrow + 12), x, y, lo);
-            row_indices8(g.rowrank, __ldg(nrow + 14), x, y, hi);
+            row_indices8(g.leaves, __ldg(nrow + 12), x, y, lo);
+            row_indices8(g.leaves, __ldg(nrow + 14), x, y, hi);
             if constexpr (VALUES) {
 #pragma unroll
                 for (int z = 0; z < 3; ++z) {
