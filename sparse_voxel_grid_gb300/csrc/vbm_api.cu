@@ -81,8 +81,10 @@ int upload(vbm_grid* g, cudaStream_t stream) {
         e = cudaMemcpyAsync(base + lay.off[i], src[i], lay.bytes[i], cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return fail_cuda("vbm_build: cudaMemcpyAsync", e);
     }
-    e = vbm::launch_row_ranks(reinterpret_cast<const vbm::LeafRec*>(base + lay.off[0]), (uint32_t)g->leaves.size(),
-                              reinterpret_cast<uint2*>(base + lay.off[7]), stream);
+    e = vbm::launch_row_ranks(reinterpret_cast<const vbm::LeafRec*>(base + lay.off[0]),
+                              reinterpret_cast<const uint32_t*>(base + lay.off[6]), (uint32_t)g->leaves.size(),
+                              reinterpret_cast<uint2*>(base + lay.off[7]), reinterpret_cast<uint4*>(base + lay.off[8]),
+                              stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: row ranks", e);
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail_cuda("vbm_build: cudaStreamSynchronize", e);

@@ -264,15 +264,30 @@ __global__ void nbr_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, uint
 }
 
 // 5e. Spans: max and the number of blocks over MaxCachedLeaves.
-// Row ranks (kRowRanks): one (leaf, row) entry per thread, grid-stride.
-__global__ void rowrank_kernel(const LeafRec* __restrict__ leaves, uint32_t nl, uint2* __restrict__ rowrank) {
+// Index of in-leaf bit `bit` (0..511) of leaf L, 0 if L is absent or the bit clear.
+__device__ __forceinline__ uint32_t index_of_bit(const LeafRec* __restrict__ leaves, uint32_t L, uint32_t bit) {
+    if (L == kNone) return 0u;
+    const uint64_t word = leaves[L].mask[bit >> 6];
+    const uint32_t b = bit & 63u;
+    return ((word >> b) & 1ull) ? leaves[L].base[bit >> 6] + (uint32_t)__popcll(word & ((1ull << b) - 1ull)) : 0u;
+}
+
+// Row ranks, with and without the z halo (kRowRanks): one (leaf, row) entry
+// per thread, grid-stride.  The z neighbours come from the leaf's neighbour row
+// (slots 12 and 14: offsets (0,0,-1) and (0,0,+1)).
+__global__ void rowrank_kernel(const LeafRec* __restrict__ leaves, const uint32_t* __restrict__ nbr, uint32_t nl,
+                               uint2* __restrict__ rowrank, uint4* __restrict__ rowrank_z) {
     const uint64_t total = (uint64_t)nl * kRowRanks, stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
-        const LeafRec& r = leaves[e >> 6];
-        const uint32_t x = (uint32_t)(e >> 3) & 7u, shift = 8u * ((uint32_t)e & 7u);
+        const uint32_t L = (uint32_t)(e >> 6), xy = (uint32_t)e & 63u;  // xy = x*8 + y
+        const LeafRec& r = leaves[L];
+        const uint32_t x = xy >> 3, shift = 8u * (xy & 7u);
         const uint64_t word = r.mask[x];
-        rowrank[e] = make_uint2(r.base[x] + (uint32_t)__popcll(word & ((1ull << shift) - 1ull)),
-                                (uint32_t)(word >> shift) & 0xFFu);
+        const uint32_t first = r.base[x] + (uint32_t)__popcll(word & ((1ull << shift) - 1ull));
+        const uint32_t bits = (uint32_t)(word >> shift) & 0xFFu;
+        const uint32_t Lm = nbr[(size_t)L * kNbrStride + 12], Lp = nbr[(size_t)L * kNbrStride + 14];
+        rowrank[e] = make_uint2(first, bits);
+        rowrank_z[e] = make_uint4(first, bits, index_of_bit(leaves, Lm, xy * 8u + 7u), index_of_bit(leaves, Lp, xy * 8u));
     }
 }
 
@@ -506,7 +521,7 @@ int build_device(const int32_t* coords, uint64_t n, int log2w, uint32_t flags, v
         nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
                                                                                  final_of, nbr);
         rowrank_kernel<<<grid_for((uint64_t)nl * kRowRanks, sm), kThreads, 0, st>>>(
-            leaves, nl, reinterpret_cast<uint2*>(base + lay.off[7]));
+            leaves, nbr, nl, reinterpret_cast<uint2*>(base + lay.off[7]), reinterpret_cast<uint4*>(base + lay.off[8]));
         span_kernel<<<grid_for(g->n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)g->n_blocks, words, ctr + 3);
         VBM_CK(cudaGetLastError());
     }
@@ -713,7 +728,7 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
         nbr_kernel<<<grid_for((uint64_t)nl * kNbrStride, sm), kThreads, 0, st>>>(leaves, nl, keys, cap - 1, slot_id,
                                                                                  final_of, nbr);
         rowrank_kernel<<<grid_for((uint64_t)nl * kRowRanks, sm), kThreads, 0, st>>>(
-            leaves, nl, reinterpret_cast<uint2*>(base + lay.off[7]));
+            leaves, nbr, nl, reinterpret_cast<uint2*>(base + lay.off[7]), reinterpret_cast<uint4*>(base + lay.off[8]));
         span_kernel<<<grid_for(n_blocks, sm), kThreads, 0, st>>>(jump, (uint32_t)n_blocks, words, ctr + 3);
         VBM_CK(cudaGetLastError());
     }
@@ -727,13 +742,15 @@ int build_device_noalloc(const int32_t* coords, uint64_t n, int log2w, uint32_t 
     return VBM_OK;
 }
 
-cudaError_t launch_row_ranks(const LeafRec* leaves, uint32_t n_leaves, uint2* rowrank, cudaStream_t stream) {
+cudaError_t launch_row_ranks(const LeafRec* leaves, const uint32_t* nbr, uint32_t n_leaves, uint2* rowrank,
+                             uint4* rowrank_z, cudaStream_t stream) {
     if (!n_leaves) return cudaSuccess;
     int device = 0, sm = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    rowrank_kernel<<<grid_for((uint64_t)n_leaves * kRowRanks, sm), kThreads, 0, stream>>>(leaves, n_leaves, rowrank);
+    rowrank_kernel<<<grid_for((uint64_t)n_leaves * kRowRanks, sm), kThreads, 0, stream>>>(leaves, nbr, n_leaves, rowrank,
+                                                                                          rowrank_z);
     return cudaGetLastError();
 }
 

@@ -35,6 +35,11 @@ constexpr int kNbrStride = 32;              // neighbour-row stride: 27 ids + 5 
 // row's first active voxel has or would have (the leaf's first index plus the
 // active voxels before the row in leaf order).  A finer copy of the leaf's
 // rank directory, derived from the masks on the device after every build.
+// rowrank_z holds the same rows with their z halo, 16 bytes each: .x, .y as
+// above, .z = the index of (x, y, -1), i.e. voxel (x,y,7) of the -z neighbour
+// leaf, .w = the index of (x, y, 8), voxel (x,y,0) of the +z neighbour (0 where
+// that voxel is inactive or its leaf absent), so that one load ranks a whole
+// three-tap z column.
 constexpr int kRowRanks = 64;
 
 // One leaf: 128 bytes, one cache line.  `mask` is the 512-bit value mask (bit
@@ -72,6 +77,7 @@ struct DevGrid {
     const uint64_t* jump;        // n_blocks x (W/64)
     const uint32_t* nbr;         // n_leaves x kNbrStride: neighbour-leaf ids (see vbm_build.cpp)
     const uint2* rowrank;        // n_leaves x 64: row ranks of each leaf (see kRowRanks)
+    const uint4* rowrank_z;      // n_leaves x 64: the same rows with their z halo (see kRowRanks)
     uint32_t n;                  // active voxels
     uint32_t n_leaves;
     uint32_t n_blocks;           // blocks a launch covers (CTAs of a one-CTA-per-block kernel)
@@ -122,9 +128,10 @@ struct vbm_grid {
 namespace vbm {
 
 // Byte offsets of the grid's arrays in its one device allocation, in the order
-// leaves, root_keys, upper, lower, first_leaf, jump, nbr, rowrank (256-byte
-// aligned).  The first seven have host copies; rowrank is made on the device.
-constexpr int kArenaArrays = 8, kHostArrays = 7;
+// leaves, root_keys, upper, lower, first_leaf, jump, nbr, rowrank, rowrank_z
+// (256-byte aligned).  The first seven have host copies; the row ranks are
+// made on the device.
+constexpr int kArenaArrays = 9, kHostArrays = 7;
 struct ArenaLayout {
     size_t off[kArenaArrays];
     size_t bytes[kArenaArrays];
@@ -142,6 +149,7 @@ inline ArenaLayout arena_layout(size_t n_leaves, size_t n_upper, size_t n_lower,
     a.bytes[5] = n_blocks * words * sizeof(uint64_t);
     a.bytes[6] = n_leaves * (size_t)kNbrStride * sizeof(uint32_t);
     a.bytes[7] = n_leaves * (size_t)kRowRanks * 2 * sizeof(uint32_t);
+    a.bytes[8] = n_leaves * (size_t)kRowRanks * 4 * sizeof(uint32_t);
     size_t total = 0;
     for (int i = 0; i < kArenaArrays; ++i) {
         a.off[i] = total;
@@ -163,6 +171,7 @@ inline void set_device_views(vbm_grid* g, const ArenaLayout& a, int sm_count) {
     d.jump = reinterpret_cast<const uint64_t*>(base + a.off[5]);
     d.nbr = reinterpret_cast<const uint32_t*>(base + a.off[6]);
     d.rowrank = reinterpret_cast<const uint2*>(base + a.off[7]);
+    d.rowrank_z = reinterpret_cast<const uint4*>(base + a.off[8]);
     d.n = (uint32_t)g->n;
     d.n_leaves = (uint32_t)g->n_leaves;
     d.n_blocks = (uint32_t)g->n_blocks;

@@ -48,8 +48,10 @@ cudaError_t launch_rows(bool gather, const float* src, int C, const uint32_t* ro
 
 // Measurement probes (vbm_probe.cu, include/vbm_probe.h).
 cudaError_t launch_probe(const DevGrid& g, int kind, const float* sidecar, cudaStream_t stream);
-// Fills the row ranks (kRowRanks) of n_leaves leaf records (vbm_build_dev.cu).
-cudaError_t launch_row_ranks(const LeafRec* leaves, uint32_t n_leaves, uint2* rowrank, cudaStream_t stream);
+// Fills both row-rank tables (kRowRanks) of n_leaves leaf records and their
+// neighbour rows (vbm_build_dev.cu).
+cudaError_t launch_row_ranks(const LeafRec* leaves, const uint32_t* nbr, uint32_t n_leaves, uint2* rowrank,
+                             uint4* rowrank_z, cudaStream_t stream);
 // Per-device kernel attributes (shared-memory opt-ins), set once when a grid
 // is created on the device, outside any stream capture.
 cudaError_t prepare_device_kernels(int device);

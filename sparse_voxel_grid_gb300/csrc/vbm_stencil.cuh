@@ -110,36 +110,41 @@ struct TapResolver {
 
 // The three taps (di,dj,-1), (di,dj,0), (di,dj,+1) of a voxel at in-leaf
 // position (x,y,z), through its leaf's staged table row.  The three positions
-// lie in one z-row of one leaf -- the row (x+di, y+dj) -- so that row's rank
-// entry (kRowRanks: its 8 mask bits and the index of its first bit) and one
+// lie in one z-row (x+di, y+dj) -- of one leaf, or past its z face at z = 0
+// or 7 -- so that row's entry with its z halo (kRowRanks: its 8 mask bits, the
+// index of its first bit and the indices of its two halo voxels) and one
 // popcount of its bits below z rank all three (the z-1 bit, when set, is the
-// last of those bits; the z+1 bit follows the centre), except where z-1 or z+1
-// crosses the leaf's z face (z = 0 or 7; never both): that tap is the last or
-// first bit of the same row of the z neighbour leaf.  Written without branches
-// (the z neighbour chosen by a select, its load predicated), so that the loads
-// of all nine columns can be in flight together.
+// last of those bits; the z+1 bit follows the centre).  Only where the row's
+// leaf is absent can a face-crossing tap still be active, in the absent leaf's
+// z neighbour: that rare case takes the table entry of the neighbour and its
+// row rank.
 template <int DI, int DJ>
-__device__ __forceinline__ void cached_column(const uint2* __restrict__ rowrank, const uint32_t* __restrict__ row,
-                                              int32_t x, int32_t y, int32_t z, uint32_t (&idx)[3]) {
+__device__ __forceinline__ void cached_column(const DevGrid& g, const uint32_t* __restrict__ row, int32_t x, int32_t y,
+                                              int32_t z, uint32_t (&idx)[3]) {
     const int32_t nx = x + DI, ny = y + DJ;
     const int32_t sxy = ((nx >> 3) + 1) * 9 + ((ny >> 3) + 1) * 3;
     const uint32_t r = (uint32_t)(nx & 7) * 8u + (uint32_t)(ny & 7), zu = (uint32_t)z;
     const bool lo = zu == 0u, hi = zu == 7u;
     const uint32_t L0 = row[sxy + 1];
-    const uint32_t Le = (lo || hi) ? row[sxy + (lo ? 0 : 2)] : kNone;
-    uint2 c = make_uint2(0u, 0u), e = make_uint2(0u, 0u);
-    if (L0 != kNone) c = __ldg(&rowrank[(size_t)L0 * kRowRanks + r]);
-    if (Le != kNone) e = __ldg(&rowrank[(size_t)Le * kRowRanks + r]);
+    uint4 c = make_uint4(0u, 0u, 0u, 0u);
+    if (L0 != kNone) {
+        c = __ldg(&g.rowrank_z[(size_t)L0 * kRowRanks + r]);
+    } else if (lo || hi) {
+        const uint32_t Le = row[sxy + (lo ? 0 : 2)];
+        if (Le != kNone) {
+            const uint2 n = __ldg(&g.rowrank[(size_t)Le * kRowRanks + r]);
+            // bit 7 of the -z neighbour's row (after its bits 0..6), or bit 0 of the +z neighbour's
+            const uint32_t t = lo ? (((n.y >> 7) & 1u) ? n.x + (uint32_t)__popc(n.y & 0x7Fu) : 0u)
+                                  : ((n.y & 1u) ? n.x : 0u);
+            c.z = t; c.w = t;
+        }
+    }
     const uint32_t cnt = (uint32_t)__popc(c.y & ((1u << zu) - 1u));  // row bits below the centre
     const uint32_t b3 = ((c.y << 1) >> zu) & 7u;                    // bits z-1, z, z+1 (0 past the row's ends)
     const uint32_t bz = (b3 >> 1) & 1u;
-    // Face-crossing tap: bit 7 of the -z neighbour's row (after its bits 0..6),
-    // or bit 0 of the +z neighbour's row.
-    const uint32_t te = lo ? (((e.y >> 7) & 1u) ? e.x + (uint32_t)__popc(e.y & 0x7Fu) : 0u)
-                           : ((e.y & 1u) ? e.x : 0u);
     idx[1] = bz ? c.x + cnt : 0u;
-    idx[0] = lo ? te : ((b3 & 1u) ? c.x + cnt - 1u : 0u);
-    idx[2] = hi ? te : ((b3 & 4u) ? c.x + cnt + bz : 0u);
+    idx[0] = lo ? c.z : ((b3 & 1u) ? c.x + cnt - 1u : 0u);
+    idx[2] = hi ? c.w : ((b3 & 4u) ? c.x + cnt + bz : 0u);
 }
 
 // The 27 box taps of one voxel in tap order, three at a time: column
@@ -147,7 +152,7 @@ __device__ __forceinline__ void cached_column(const uint2* __restrict__ rowrank,
 template <int C3>
 __device__ __forceinline__ void box_column(const DevGrid& g, const uint32_t* table_row, int32_t x, int32_t y,
                                            int32_t z, uint32_t (&idx)[3]) {
-    cached_column<C3 / 3 - 1, C3 % 3 - 1>(g.rowrank, table_row, x, y, z, idx);
+    cached_column<C3 / 3 - 1, C3 % 3 - 1>(g, table_row, x, y, z, idx);
 }
 
 // 27-tap box filter of one voxel ([2262] "What changed"): taps in order
