@@ -36,6 +36,20 @@ def _extreme():
     return np.unique(np.concatenate(parts), axis=0).astype(np.int32)
 
 
+def _absent_edge_leaves():
+    # Taps that cross a leaf's x or y face and its z face at once, into a leaf
+    # whose edge-sharing neighbour (the one across the x or y face only) is
+    # absent: the tap is active although its z-row's own leaf does not exist.
+    rng = np.random.default_rng(21)
+    own = np.argwhere(rng.random((8, 8, 8)) < 0.3).astype(np.int32)
+    fixed = [(7, 3, 0), (7, 3, 7), (3, 7, 0), (3, 7, 7), (0, 0, 0), (7, 7, 7), (0, 4, 0),  # leaf (0,0,0)
+             (8, 3, -1), (8, 3, 8), (9, 2, -3),          # leaves (1,0,-1), (1,0,1)
+             (3, 8, -1), (3, 8, 8), (2, 12, 9),          # leaves (0,1,-1), (0,1,1)
+             (-1, -1, -1), (-4, -6, -2), (8, 8, 8),      # leaves (-1,-1,-1), (1,1,1)
+             (-1, 4, -1), (-1, 4, -8)]                   # leaf (-1,0,-1)
+    return np.unique(np.concatenate([own, np.array(fixed, dtype=np.int32)]), axis=0).astype(np.int32)
+
+
 SMALL = dict(GRIDS)
 SMALL.update({
     "extreme": _extreme,
@@ -43,6 +57,7 @@ SMALL.update({
     "single": _single,
     "exact_blocks": _exact_blocks,
     "exact_plus_one": lambda: _exact_blocks(257),
+    "absent_edge_leaves": _absent_edge_leaves,
 })
 
 RESOLVERS = [vbm.RESOLVE_TREEWALK, vbm.RESOLVE_CACHED, vbm.RESOLVE_BRICK]
