@@ -52,10 +52,12 @@ __device__ __forceinline__ void box_filter_block(const DevGrid& g, const float* 
     if (b == 0 && threadIdx.x < (unsigned)CC) out[ch0 + threadIdx.x] = 0.0f;
 }
 
-// The streamed one-lane forms (CC <= 3) run held to 40 registers (3 CTAs of 512
-// threads, 12 of 128, per SM): left free, the cached C=1 kernel takes 54 and
-// runs 7-15% slower with fewer CTAs resident.  The wider and materialised forms
-// would spill under that cap and keep the compiler's choice.
+// The streamed one-lane forms (CC <= 3) run under a register bound: the cached
+// ones at 32 (4 CTAs of 512 threads, 16 of 128, per SM; 48.7-49.2 against
+// 51.2 us at 40 for C=1 on the 1.29M-voxel shell at W=128), the tree-walk ones
+// at 40 (they spill at 32).  Left free, the cached C=1 kernel took 54 and ran
+// 7-15% slower with fewer CTAs resident.  The wider and materialised forms
+// would spill under these caps and keep the compiler's choice.
 template <int CC, bool VEC, bool CACHED, bool MAT, int CT>
 __global__ void __launch_bounds__(512) box_filter_kernel(DevGrid g, const float* __restrict__ sc,
                                                          float* __restrict__ out, int C, int ch0) {
